@@ -1,0 +1,487 @@
+"""Decode-step benchmark: TidalDecode PPSA schedule vs the all-full schedule.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--top-k K]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+One "step" is one decode step of the whole L-layer attention-only stack
+(full, full+select and sparse layers per the review's Figure 2 schedule) over
+one batch of synthetic, seeded inputs resident in HBM.  Default workload: the
+LLaMA-2-7B attention shape at 10K context (batch 1, 32 layers, 32 heads,
+d=128, N=10240, k=512, selection at L2 and L7).
+
+Timing: W untimed warm-up steps, then exactly K timed steps, each preceded by
+an L2 flush (a 1 GiB device write, outside the timed events), timed with CUDA
+events on the launching stream, bracketed by a barrier and a device sync;
+the max over ranks is reported.  Pass 1 replays the step as a captured CUDA
+graph (the headline latency); pass 2 runs the same K steps through
+td_decode_step with per-layer events (per-kernel durations, roofline).
+`--impl reference` times the CPU oracle instead (host cores, bounded sample).
+Multi-GPU (torchrun): independent replicas, one per GPU, no collective on the
+data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = ("decode-step attention latency (us) and achieved KV HBM GB/s vs peak, PPSA vs full")
+DEFAULT_CONFIG = "llama2-7b-10k"
+FLUSH_BYTES = 1 << 30
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ----------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def dist_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity on one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------- byte model
+def step_bytes(wl: W.Workload, lens: np.ndarray, modes) -> dict:
+    """Algorithmic HBM bytes of one step: K/V rows touched (512 B per token per
+    KV head at d=128), plus q/out and the index/score traffic listed apart."""
+    d, Hkv, Hq, B = wl.head_dim, wl.kv_heads, wl.q_heads, wl.batch
+    row = 2 * d * 2                                          # K + V bf16 per token
+    full_kv = int(np.sum(lens)) * Hkv * row
+    k_eff = np.minimum(lens, wl.top_k)
+    sparse_kv = int(np.sum(k_eff)) * Hkv * row
+    qo = B * Hq * d * 2 * 2                                  # q read + out write
+    per = {"full": full_kv + qo, "sparse": sparse_kv + qo + B * Hkv * wl.top_k * 4}
+    kv = {"full": full_kv, "sparse": sparse_kv}
+    total_kv = sum(kv["sparse"] if m == W.SPARSE else kv["full"] for m in modes)
+    return {"per_launch": per, "kv": kv, "step_kv": total_kv}
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- oracle timing
+def oracle_sample(wl: W.Workload, host_layers, lens, n_groups: int, modes):
+    """Time the CPU oracle on n_groups sampled (batch row, KV head) groups over
+    all layers; returns (seconds for the sample, groups timed, threads)."""
+    import oracle
+    orc = oracle.get()
+    G = wl.group
+    rs = np.random.RandomState(wl.seed + 5)
+    all_groups = [(b, g) for b in range(wl.batch) for g in range(wl.kv_heads)]
+    pick = [all_groups[i] for i in sorted(rs.choice(len(all_groups),
+                                                    size=min(n_groups, len(all_groups)),
+                                                    replace=False))]
+    nmax = int(max(lens[b] for b, _ in pick))
+    qs, Ks, Vs = [], [], []
+    for (qh, Kh, Vh) in host_layers:
+        qs.append(np.ascontiguousarray(np.stack([qh[b, g * G:(g + 1) * G] for b, g in pick])))
+        Ks.append(np.ascontiguousarray(np.stack([Kh[b, g:g + 1, :nmax] for b, g in pick])))
+        Vs.append(np.ascontiguousarray(np.stack([Vh[b, g:g + 1, :nmax] for b, g in pick])))
+    sl = np.array([lens[b] for b, _ in pick], np.int32)
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(wl.head_dim)))
+    t0 = time.perf_counter()
+    _, _, rc = orc.decode_step(list(modes), qs, Ks, Vs, sl, wl.top_k, scale)
+    dt = time.perf_counter() - t0
+    if rc:
+        raise RuntimeError(f"oracle failed: {rc}")
+    return dt, len(pick), orc.num_threads()
+
+
+def host_copies(layers, wl, n_groups):
+    """bf16 bit patterns on the host for the oracle (whole tensors; the sample
+    is cut from them)."""
+    return [(W.u16(q), W.u16(K), W.u16(V)) for q, K, V in layers]
+
+
+# ----------------------------------------------------------------- helpers
+def load_measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def attn_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("td_attn.cu", "td_internal.h"):
+        with open(os.path.join(ROOT, "sparse_attention_td_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the full-attention kernel from a committed ncu
+    summary, or None if there is none for this workload or the kernel source
+    changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("source_hash") != attn_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+    import sparse_attention_td_gb300 as td
+    if not os.path.exists(td.lib_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+
+    wl = W.WORKLOADS[args.config]
+    if args.top_k:
+        wl = wl.with_(top_k=args.top_k)
+    heavy = W.heavy_positions(wl)
+    lens = W.seq_lens(wl)
+    layers = [W.generate_layer(wl, layer, device, heavy[layer]) for layer in range(wl.layers)]
+    q = [x[0] for x in layers]
+    K = [x[1] for x in layers]
+    V = [x[2] for x in layers]
+    seq = torch.as_tensor(lens).to(device)
+    shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len,
+                          scale=td.default_scale(wl.head_dim))
+    outs = [torch.empty_like(x) for x in q]
+    idx = torch.full((wl.batch, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device=device)
+    ws = td.Workspace(shape, wl.top_k, device=device)
+    modes = list(wl.modes)
+    full_modes = list(W.all_full_schedule(wl.layers))
+    plan = td.Plan(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
+    plan_full = td.Plan(shape, full_modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    K_steps, W_steps = args.steps, args.warmup
+
+    def flush_l2():
+        flush.fill_(1.0)
+
+    def graph_pass(p, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            flush_l2()
+            a.record(stream)
+            p.launch(stream)
+            b.record(stream)
+        return ev
+
+    # warm-up
+    for _ in range(W_steps):
+        flush_l2()
+        plan.launch(stream)
+        flush_l2()
+        plan_full.launch(stream)
+        td.td_decode_step(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws,
+                          stream=stream)
+    torch.cuda.synchronize(device)
+
+    # pass 1: the step as a graph (headline), then the all-full schedule
+    with ClockSampler(local) as clocks:
+        dist_barrier(world, device)
+        torch.cuda.synchronize(device)
+        t_wall = time.perf_counter()
+        ev_ppsa = graph_pass(plan, K_steps)
+        torch.cuda.synchronize(device)
+        wall_ppsa = time.perf_counter() - t_wall
+        dist_barrier(world, device)
+        ev_full = graph_pass(plan_full, K_steps)
+        torch.cuda.synchronize(device)
+        dist_barrier(world, device)
+        # pass 2: per-layer events around each layer's launches
+        traced = []
+        for _ in range(K_steps):
+            flush_l2()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(wl.layers + 1)]
+            td.td_decode_step(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws,
+                              stream=stream, layer_events=e)
+            traced.append(e)
+        torch.cuda.synchronize(device)
+        dist_barrier(world, device)
+    ppsa_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_ppsa) * 1e3
+    full_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_full) * 1e3
+    per_layer = np.array([[e[i].elapsed_time(e[i + 1]) * 1e3 for i in range(wl.layers)]
+                          for e in traced])                      # [K, L] us
+    traced_step_us = float(np.mean([e[0].elapsed_time(e[-1]) * 1e3 for e in traced]))
+    layer_mean = per_layer.mean(axis=0)
+    by_mode = {}
+    for name, m in (("full", W.FULL), ("full_select", W.FULL_SELECT), ("sparse", W.SPARSE)):
+        sel = [i for i, mm in enumerate(modes) if mm == m]
+        if sel:
+            by_mode[name] = float(np.mean(layer_mean[sel]))
+    ppsa_us = dist_max(ppsa_us, world, device)
+    full_us = dist_max(full_us, world, device)
+
+    # e2e: host q in (pinned), graph step, host outputs back, per step
+    q_host = [x.cpu().pin_memory() for x in q]
+    o_host = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
+    h2d = sum(x.numel() * x.element_size() for x in q_host)
+    d2h = sum(x.numel() * x.element_size() for x in o_host)
+    for _ in range(max(W_steps, 1)):
+        for src, dst in zip(q_host, q):
+            dst.copy_(src, non_blocking=True)
+        plan.launch(stream)
+        for src, dst in zip(outs, o_host):
+            dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize(device)
+    dist_barrier(world, device)
+    e2e_ev = []
+    for _ in range(K_steps):
+        flush_l2()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for src, dst in zip(q_host, q):
+            dst.copy_(src, non_blocking=True)
+        plan.launch(stream)
+        for src, dst in zip(outs, o_host):
+            dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        e2e_ev.append((a, b))
+    torch.cuda.synchronize(device)
+    e2e_us = dist_max(statistics.fmean(a.elapsed_time(b) for a, b in e2e_ev) * 1e3, world, device)
+    assert ws.status() == 0, "device status word set during the bench"
+
+    bytes_model = step_bytes(wl, lens, modes)
+    peaks, peak_kind = load_measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    full_launch_us = by_mode.get("full", by_mode.get("full_select"))
+    achieved = bytes_model["per_launch"]["full"] / (full_launch_us * 1e-6) / 1e9
+    sparse_gbs = (bytes_model["per_launch"]["sparse"] / (by_mode["sparse"] * 1e-6) / 1e9
+                  if "sparse" in by_mode else None)
+    traffic = measured_traffic(wl.name)
+    launches_per_step = sum(2 if m == W.FULL_SELECT else 1 for m in modes)
+
+    result = None
+    if rank == 0:
+        result = {
+            "metric": METRIC,
+            "value": round(ppsa_us, 2),
+            "unit": "us",
+            "n_gpus": world,
+            "steps": K_steps,
+            "warmup": W_steps,
+            "ms_per_step": round(ppsa_us / 1e3, 5),
+            "higher_is_better": False,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 K/V/q with planted heavy positions)",
+            "config": {
+                "workload": wl.name, "batch": wl.batch, "layers": wl.layers,
+                "q_heads": wl.q_heads, "kv_heads": wl.kv_heads, "head_dim": wl.head_dim,
+                "seq_len": wl.max_seq_len, "seq_len_sum": int(np.sum(lens)), "top_k": wl.top_k,
+                "schedule": "".join("FSP"[m] for m in modes),
+                "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
+                "parallelism": f"replicas x{world}",
+                "timing": "CUDA-graph step, CUDA events on the launching stream, mean of K",
+            },
+            "kv_bytes_per_step": bytes_model["step_kv"],
+            "kv_gbs": round(bytes_model["step_kv"] / (ppsa_us * 1e-6) / 1e9, 1),
+            "kv_frac_of_peak": round(bytes_model["step_kv"] / (ppsa_us * 1e-6) / 1e9 / peak, 4),
+            "all_full_us": round(full_us, 2),
+            "all_full_kv_gbs": round(bytes_model["kv"]["full"] * wl.layers / (full_us * 1e-6) / 1e9,
+                                     1),
+            "speedup_vs_all_full": round(full_us / ppsa_us, 3),
+            "traced_step_us": round(traced_step_us, 2),
+            "layer_us": {k: round(v, 2) for k, v in by_mode.items()},
+            "sparse_layer_gbs": round(sparse_gbs, 1) if sparse_gbs else None,
+            "roofline": {
+                "kernel": "attention_kernel<G,full> (full layer: split-K flash decode + combine)",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": bytes_model["per_launch"]["full"],
+                "launch_us": round(full_launch_us, 2),
+            },
+            "gpu_launches": launches_per_step * K_steps,
+            "e2e": {"value": round(e2e_us, 2), "unit": "us", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "clocks": clocks.summary(),
+            "wall_s_pass1": round(wall_ppsa, 3),
+        }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = host_copies(layers, wl, args.cpu_groups)
+        groups = wl.batch * wl.kv_heads
+        secs, n_done, threads, reps = 0.0, 0, 1, 0
+        while secs < args.cpu_seconds and reps < 50:
+            dt, n_done, threads = oracle_sample(wl, host, lens, args.cpu_groups, modes)
+            secs += dt
+            reps += 1
+        per_step_us = secs / reps * (groups / n_done) * 1e6
+        result["cpu_baseline"] = {
+            "value": round(per_step_us, 1), "unit": "us", "cores": threads, "kind": "oracle",
+            "sample": f"{n_done} of {groups} (batch row, KV head) groups through all "
+                      f"{wl.layers} layers, x{reps} runs, scaled to the whole step",
+        }
+    return result
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return None
+    import torch
+    wl = W.WORKLOADS[args.config]
+    if args.top_k:
+        wl = wl.with_(top_k=args.top_k)
+    heavy = W.heavy_positions(wl)
+    lens = W.seq_lens(wl)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    layers = [W.generate_layer(wl, layer, dev, heavy[layer]) for layer in range(wl.layers)]
+    host = host_copies(layers, wl, args.cpu_groups)
+    del layers
+    groups = wl.batch * wl.kv_heads
+    times, threads, n_done = [], 1, 0
+    for i in range(args.warmup + args.steps):
+        dt, n_done, threads = oracle_sample(wl, host, lens, args.cpu_groups, wl.modes)
+        if i >= args.warmup:
+            times.append(dt * (groups / n_done) * 1e6)
+    value = statistics.fmean(times)
+    sample = (f"{n_done} of {groups} (batch row, KV head) groups through all {wl.layers} layers "
+              f"per step, scaled to the whole step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "us",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "layers": wl.layers,
+                   "q_heads": wl.q_heads, "kv_heads": wl.kv_heads, "seq_len": wl.max_seq_len,
+                   "top_k": wl.top_k, "parallelism": "host cores (oracle)"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": "us", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--top-k", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-groups", type=int, default=16)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank, local)
+    else:
+        res = run_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

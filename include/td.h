@@ -1,0 +1,208 @@
+/*
+ * td.h -- C ABI of the GB300 (sm_103a) decode-step library for TidalDecode's
+ * Position Persistent Sparse Attention (PPSA).
+ *
+ * The method (TidalDecode: Fast and Accurate LLM Decoding with Position
+ * Persistent Sparse Attention -- paper review page):
+ *   - §三 "Position Persistent Sparse Attention": A = q K^T / sqrt(d),
+ *     H = softmax(A) V per layer and head; sparse layers reuse the token
+ *     positions chosen by the most recent selection layer instead of
+ *     selecting per layer and head.
+ *   - §二 "core insight" and §三 Figure 2: each decode step runs full
+ *     attention at the first layers, full attention + top-k token selection
+ *     at layer 2 and at one middle layer, and PPSA (sparse attention over the
+ *     persisted positions) everywhere else.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller; the
+ *     library never allocates device memory on these paths.  Scratch comes
+ *     from a caller-owned workspace of td_workspace_size() bytes that was
+ *     zeroed once by td_workspace_init() (kernels leave it re-usable).
+ *   - Layouts (row-major, contiguous):
+ *       q          [batch][num_q_heads][head_dim]                 bf16
+ *       k/v cache  [batch][num_kv_heads][max_seq_len][head_dim]   bf16
+ *       seq_lens   [batch]                                        int32 (device)
+ *       out        [batch][num_q_heads][head_dim]                 bf16
+ *       out_f32    [batch][num_q_heads][head_dim]                 fp32 (optional)
+ *       idx        [batch][num_kv_heads][top_k]                   int32
+ *       scores     [batch][num_kv_heads][max_seq_len]             fp32 (optional)
+ *     Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *     q, k, v, out and out_f32 must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = legacy default stream).  Outputs are valid once the stream has
+ *     reached the end of the call.  Calls that share a workspace must be
+ *     ordered on one stream.
+ *   - Errors: argument, shape and schedule errors are detected on the host
+ *     before anything is launched and returned synchronously.  A failed
+ *     launch returns TD_ERR_CUDA.  Device-side input errors (an index at or
+ *     beyond seq_lens[b], a seq_lens entry outside [0, max_seq_len]) never
+ *     fault: the offending entry is skipped or clamped and a bit is set in
+ *     the workspace status word, read with td_workspace_status().
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef TD_H_
+#define TD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TD_OK = 0,
+    TD_ERR_INVALID_ARG = 1,         /* null/misaligned pointer, bad count or mode */
+    TD_ERR_UNSUPPORTED_SHAPE = 2,   /* head_dim != 128, group size not 1/2/4/8, ... */
+    TD_ERR_NO_SELECTION = 3,        /* sparse layer with no persisted index set */
+    TD_ERR_WORKSPACE_TOO_SMALL = 4,
+    TD_ERR_CUDA = 5                 /* a CUDA runtime call or launch failed */
+} td_status;
+
+/* Layer modes of one decode step (review §三 Figure 2). */
+typedef enum {
+    TD_MODE_FULL = 0,          /* full attention, no selection            */
+    TD_MODE_FULL_SELECT = 1,   /* full attention + top-k token selection  */
+    TD_MODE_SPARSE = 2         /* PPSA: attention over the persisted set  */
+} td_layer_mode;
+
+/* Bits of the device status word (td_workspace_status). */
+#define TD_FLAG_INDEX_OUT_OF_RANGE 0x1u   /* idx entry < -1 or >= seq_lens[b]: skipped */
+#define TD_FLAG_SEQ_LEN_OUT_OF_RANGE 0x2u /* seq_lens[b] < 0 or > max_seq_len: clamped */
+
+typedef struct {
+    int32_t batch;          /* B  >= 1                                         */
+    int32_t num_q_heads;    /* Hq >= 1, a multiple of num_kv_heads             */
+    int32_t num_kv_heads;   /* Hkv >= 1; Hq / Hkv must be 1, 2, 4 or 8         */
+    int32_t head_dim;       /* d; only 128 is supported                        */
+    int32_t max_seq_len;    /* N_max: token rows per (batch, KV head) in K/V   */
+    float scale;            /* softmax scale; 0 selects 1/sqrtf(head_dim)      */
+} td_shape;
+
+/* Human-readable name of a status code (static storage). */
+const char *td_status_string(td_status status);
+
+/* Bytes of workspace needed by every call below for this shape and top_k
+ * (top_k = 0 when no call selects or runs sparse attention).  Returns 0 for
+ * an invalid shape.  Does not touch the GPU. */
+size_t td_workspace_size(const td_shape *shape, int32_t top_k);
+
+/* Zero a freshly allocated workspace (a cudaMemsetAsync on `stream`).  Must
+ * be called once before the workspace's first use; the kernels leave it
+ * in the same state after every call. */
+td_status td_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronise `stream`, copy the device status word into *flags
+ * (TD_FLAG_* bits, 0 = clean) and clear it. */
+td_status td_workspace_status(void *ws, size_t ws_bytes, uint32_t *flags, void *stream);
+
+/*
+ * One full-attention layer, optionally with token selection (review §三
+ * Figure 2 rows "Full Attention" and "Full Attention + Token Selection").
+ *   For every batch row b and query head h, with a[n] = scale * q[b,h] . K[b,g(h),n]
+ *   for n < seq_lens[b]:   out[b,h] = sum_n softmax(a)[n] * V[b,g(h),n].
+ *   top_k > 0 also selects, per (b, KV head g), the top_k positions by the
+ *   summed score s[n] = sum over the query heads h of g of a_h[n]; ties go
+ *   to the lower position; idx_out[b,g,:] receives them in ascending order,
+ *   padded with -1 when seq_lens[b] < top_k.
+ *   top_k = 0: no selection (idx_out may be NULL).
+ *   out_f32 (optional) receives the fp32 result before rounding to bf16.
+ *   scores_out (optional, fp32 [B][Hkv][max_seq_len]) receives s[n] for
+ *   n < seq_lens[b] when top_k > 0 (other entries untouched).
+ *   A batch row with seq_lens[b] = 0 gets out = 0.
+ */
+td_status td_full_attn_select(const td_shape *shape, const void *q, const void *k_cache,
+                              const void *v_cache, const int32_t *seq_lens, int32_t top_k,
+                              int32_t *idx_out, void *out, float *out_f32, float *scores_out,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The selection step of a FULL_SELECT layer on its own, from caller-provided
+ * scores (review §二 core insight: keep the tokens with the highest
+ * attention scores; §三 Figure 2 "Token Selection -> top-k tokens").
+ *   scores   device fp32 [B][Hkv][max_seq_len]; entries n < seq_lens[b] are read.
+ *   idx_out  device int32 [B][Hkv][top_k]: per (b, g) the top_k positions of
+ *            the largest scores, ties to the lower position, ascending,
+ *            padded with -1 when seq_lens[b] < top_k.  -0.0 ties with +0.0;
+ *            NaN scores give an unspecified (but in-range) selection.
+ *   top_k >= 1.  The workspace is used for its status word only.
+ */
+td_status td_topk_select(const td_shape *shape, const float *scores, const int32_t *seq_lens,
+                         int32_t top_k, int32_t *idx_out, void *ws, size_t ws_bytes,
+                         void *stream);
+
+/*
+ * One PPSA layer (review §三 "Position Persistent Sparse Attention"):
+ *   attention of every query head over the positions idx[b,g(h),0..top_k)
+ *   only (entries of -1 are padding and are skipped), with the softmax
+ *   normalised over those positions.  An all-padding row gives out = 0.
+ *   idx entries must be distinct; their order does not matter.
+ */
+td_status td_sparse_attn(const td_shape *shape, const void *q, const void *k_cache,
+                         const void *v_cache, const int32_t *seq_lens, const int32_t *idx,
+                         int32_t top_k, void *out, float *out_f32, void *ws, size_t ws_bytes,
+                         void *stream);
+
+/*
+ * One decode step over an L-layer attention-only stack (review §三 Figure 2).
+ *   modes       HOST array [num_layers] of td_layer_mode.
+ *   q, k_caches, v_caches, outs   HOST arrays of num_layers device pointers
+ *               (one layer's tensors each, layouts as above).
+ *   outs_f32    HOST array of num_layers device pointers (entries may be
+ *               NULL), or NULL.
+ *   idx_buf     device [B][Hkv][top_k]: the persisted index set.  Every
+ *               FULL_SELECT layer overwrites it; every SPARSE layer reads the
+ *               set of the most recent FULL_SELECT before it.  It stays on
+ *               the device across layers and after the call.
+ *   idx_valid   nonzero if idx_buf already holds a set on entry; otherwise a
+ *               SPARSE layer before the first FULL_SELECT is rejected with
+ *               TD_ERR_NO_SELECTION (nothing is launched).
+ *   layer_events  optional HOST array of num_layers + 1 cudaEvent_t (as
+ *               void*): event l is recorded on `stream` before layer l and
+ *               event num_layers after the last layer (per-layer timing).
+ * No host synchronisation happens inside the call; it can be captured into a
+ * CUDA graph (see td_plan_create).
+ */
+td_status td_decode_step(const td_shape *shape, int32_t num_layers, const int32_t *modes,
+                         const void *const *q, const void *const *k_caches,
+                         const void *const *v_caches, const int32_t *seq_lens, int32_t top_k,
+                         int32_t *idx_buf, int32_t idx_valid, void *const *outs,
+                         float *const *outs_f32, void *ws, size_t ws_bytes, void *stream,
+                         void *const *layer_events);
+
+/*
+ * A decode step captured once into a CUDA graph and replayed with one launch
+ * (same arguments and semantics as td_decode_step; the pointers are baked
+ * into the graph, so the buffers must stay allocated while the plan lives).
+ * Creation runs no kernel.  td_plan_launch enqueues the whole step on
+ * `stream`.  The plan holds host-side graph objects only.
+ */
+typedef struct td_plan td_plan;
+td_status td_plan_create(td_plan **plan, const td_shape *shape, int32_t num_layers,
+                         const int32_t *modes, const void *const *q,
+                         const void *const *k_caches, const void *const *v_caches,
+                         const int32_t *seq_lens, int32_t top_k, int32_t *idx_buf,
+                         int32_t idx_valid, void *const *outs, float *const *outs_f32, void *ws,
+                         size_t ws_bytes);
+td_status td_plan_launch(td_plan *plan, void *stream);
+void td_plan_destroy(td_plan *plan);
+
+/*
+ * Kernel tuning knobs (process-wide, not thread-safe; for sweeps):
+ *   "full_ctas_per_sm", "sparse_ctas_per_sm": resident CTAs assumed per SM
+ *   "full_waves", "sparse_waves": target waves of CTAs per launch
+ *   "max_splits": upper bound on splits per (batch, KV head)
+ * value <= 0 restores the default.  Unknown key -> TD_ERR_INVALID_ARG.
+ */
+td_status td_set_tuning(const char *key, int32_t value);
+
+/* Number of splits per (batch, KV head) the next full (sparse = 0) or sparse
+ * (sparse = 1) launch of this shape would use on the current device
+ * (for byte accounting and tests). */
+int32_t td_query_splits(const td_shape *shape, int32_t top_k, int32_t sparse);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TD_H_ */

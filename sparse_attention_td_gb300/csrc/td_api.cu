@@ -1,0 +1,597 @@
+// td_api.cu -- the C ABI of include/td.h: argument validation, workspace
+// layout, split planning, the per-step layer scheduler and CUDA-graph plans.
+//
+// The layer scheduler follows the decode step of the TidalDecode paper
+// review (§三 Figure 2): full layers run the attention kernel, selection
+// layers run it with score emission followed by the top-k kernel (which
+// overwrites the resident index buffer), and PPSA layers run the sparse
+// attention kernel over the most recent selection (§三 "Position Persistent
+// Sparse Attention": later layers reuse the selected positions).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+
+#include "../../include/td.h"
+#include "td_internal.h"
+
+namespace {
+
+using td::kHeadDim;
+
+struct Tuning {
+    int full_ctas_per_sm = 0;    // 0 = occupancy query
+    int sparse_ctas_per_sm = 0;
+    int full_waves = 2;
+    int sparse_waves = 1;
+    int max_splits = td::kMaxSplits;
+};
+Tuning g_tuning;
+const Tuning kDefaultTuning;
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+inline long ceil_div(long a, long b) { return (a + b - 1) / b; }
+
+// Largest split count a launch of `n_total` tokens/entries may use.
+int split_cap(long units, long n_total, bool sparse)
+{
+    long cap = g_tuning.max_splits;
+    if (cap > td::kMaxSplits)
+        cap = td::kMaxSplits;
+    const long by_len = ceil_div(n_total > 0 ? n_total : 1, td::kTokPerRound);
+    if (cap > by_len)
+        cap = by_len;
+    const long by_ctas = td::kMaxSplitCtas / units;
+    if (cap > by_ctas)
+        cap = by_ctas;
+    if (cap < 1)
+        cap = 1;
+    if (sparse) {  // a sparse CTA stages at most kMaxSparseChunk entries
+        const long need = ceil_div(n_total > 0 ? n_total : 1, td::kMaxSparseChunk);
+        if (cap < need)
+            cap = need;
+    }
+    return (int)cap;
+}
+
+// Partial-result capacity in (batch*kv_head, split) slots: covers every split
+// count split_cap can return, for any tuning.
+long partial_slots(const td_shape &s, int top_k)
+{
+    const long units = (long)s.batch * s.num_kv_heads;
+    long most = 1;
+    // Full launches: at most min(kMaxSplits, ceil(N/64), 8192/units) splits.
+    long full = ceil_div(s.max_seq_len > 0 ? s.max_seq_len : 1, td::kTokPerRound);
+    if (full > td::kMaxSplits) full = td::kMaxSplits;
+    long by_ctas = td::kMaxSplitCtas / units;
+    if (by_ctas < 1) by_ctas = 1;
+    if (full > by_ctas) full = by_ctas;
+    if (full > most) most = full;
+    if (top_k > 0) {
+        long sp = ceil_div(top_k, td::kTokPerRound);
+        if (sp > td::kMaxSplits) sp = td::kMaxSplits;
+        if (sp > by_ctas) sp = by_ctas;
+        const long need = ceil_div(top_k, td::kMaxSparseChunk);
+        if (sp < need) sp = need;
+        if (sp > most) most = sp;
+    }
+    return units * most;
+}
+
+struct WsLayout {
+    size_t status, tickets, part_m, part_l, part_o, scores, total;
+};
+
+WsLayout ws_layout(const td_shape &s, int top_k)
+{
+    const int G = s.num_q_heads / s.num_kv_heads;
+    const size_t units = (size_t)s.batch * s.num_kv_heads;
+    const size_t slots = (size_t)partial_slots(s, top_k);
+    WsLayout w{};
+    size_t off = 0;
+    w.status = off;
+    off = align_up(off + sizeof(uint32_t));
+    w.tickets = off;
+    off = align_up(off + units * sizeof(uint32_t));
+    w.part_m = off;
+    off = align_up(off + slots * G * sizeof(float));
+    w.part_l = off;
+    off = align_up(off + slots * G * sizeof(float));
+    w.part_o = off;
+    off = align_up(off + slots * G * kHeadDim * sizeof(float));
+    w.scores = off;
+    if (top_k > 0)
+        off = align_up(off + units * (size_t)s.max_seq_len * sizeof(float));
+    w.total = off;
+    return w;
+}
+
+td_status check_shape(const td_shape *s)
+{
+    if (!s)
+        return TD_ERR_INVALID_ARG;
+    if (s->batch < 1 || s->num_q_heads < 1 || s->num_kv_heads < 1 || s->max_seq_len < 1)
+        return TD_ERR_INVALID_ARG;
+    if (s->num_q_heads % s->num_kv_heads)
+        return TD_ERR_INVALID_ARG;
+    if (!isfinite(s->scale) || s->scale < 0.0f)
+        return TD_ERR_INVALID_ARG;
+    const int G = s->num_q_heads / s->num_kv_heads;
+    if (s->head_dim != kHeadDim)
+        return TD_ERR_UNSUPPORTED_SHAPE;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return TD_ERR_UNSUPPORTED_SHAPE;
+    if (s->batch > 65535 || s->num_kv_heads > 65535)
+        return TD_ERR_UNSUPPORTED_SHAPE;
+    return TD_OK;
+}
+
+float effective_scale(const td_shape &s)
+{
+    return s.scale != 0.0f ? s.scale : 1.0f / sqrtf((float)s.head_dim);
+}
+
+int device_sm_count()
+{
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 152;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Splits and per-split chunk for one launch.
+void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int &nsplit, int &chunk)
+{
+    const int G = s.num_q_heads / s.num_kv_heads;
+    const long units = (long)s.batch * s.num_kv_heads;
+    int per_sm = sparse ? g_tuning.sparse_ctas_per_sm : g_tuning.full_ctas_per_sm;
+    if (per_sm <= 0)
+        per_sm = td::attention_ctas_per_sm(G, sparse, select);
+    const int waves = sparse ? g_tuning.sparse_waves : g_tuning.full_waves;
+    const long target = (long)device_sm_count() * per_sm * (waves > 0 ? waves : 1);
+    const int cap = split_cap(units, n_total, sparse);
+    long want = ceil_div(target, units);
+    if (want < 1) want = 1;
+    if (want > cap) want = cap;
+    const long len = n_total > 0 ? n_total : 1;
+    long ch = ceil_div(ceil_div(len, want), td::kTokPerRound) * td::kTokPerRound;
+    if (sparse && ch > td::kMaxSparseChunk)
+        ch = td::kMaxSparseChunk;
+    long ns = ceil_div(len, ch);
+    if (ns > cap) {  // rounding pushed past the cap: widen the chunk instead
+        ch = ceil_div(ceil_div(len, cap), td::kTokPerRound) * td::kTokPerRound;
+        ns = ceil_div(len, ch);
+    }
+    nsplit = (int)ns;
+    chunk = (int)ch;
+}
+
+struct Ctx {
+    td_shape shape;
+    int G;
+    float scale;
+    WsLayout ws;
+    char *wsb;
+};
+
+td_status make_ctx(const td_shape *shape, int top_k, void *ws, size_t ws_bytes, Ctx &c)
+{
+    td_status st = check_shape(shape);
+    if (st)
+        return st;
+    if (top_k < 0 || top_k > shape->max_seq_len)
+        return TD_ERR_INVALID_ARG;
+    if (top_k > td::kMaxTopK)
+        return TD_ERR_UNSUPPORTED_SHAPE;
+    if (!ws || !aligned(ws, kAlign))
+        return TD_ERR_INVALID_ARG;
+    c.shape = *shape;
+    c.G = shape->num_q_heads / shape->num_kv_heads;
+    c.scale = effective_scale(*shape);
+    c.ws = ws_layout(*shape, top_k);
+    if (ws_bytes < c.ws.total)
+        return TD_ERR_WORKSPACE_TOO_SMALL;
+    c.wsb = (char *)ws;
+    return TD_OK;
+}
+
+td::AttnArgs base_args(const Ctx &c, const void *q, const void *k, const void *v,
+                       const int32_t *seq_lens, void *out, float *out_f32)
+{
+    td::AttnArgs a{};
+    a.q = (const uint16_t *)q;
+    a.k = (const uint16_t *)k;
+    a.v = (const uint16_t *)v;
+    a.seq_lens = seq_lens;
+    a.out = (uint16_t *)out;
+    a.out_f32 = out_f32;
+    a.part_m = (float *)(c.wsb + c.ws.part_m);
+    a.part_l = (float *)(c.wsb + c.ws.part_l);
+    a.part_o = (float *)(c.wsb + c.ws.part_o);
+    a.tickets = (uint32_t *)(c.wsb + c.ws.tickets);
+    a.status = (uint32_t *)(c.wsb + c.ws.status);
+    a.Hq = c.shape.num_q_heads;
+    a.Hkv = c.shape.num_kv_heads;
+    a.Nmax = c.shape.max_seq_len;
+    a.scale = c.scale;
+    return a;
+}
+
+td_status check_layer_ptrs(const void *q, const void *k, const void *v, const void *out,
+                           const float *out_f32)
+{
+    if (!q || !k || !v || !out)
+        return TD_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+        return TD_ERR_INVALID_ARG;
+    if (out_f32 && !aligned(out_f32, 16))
+        return TD_ERR_INVALID_ARG;
+    return TD_OK;
+}
+
+// Launches of one full(+select) layer; arguments already validated.
+td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
+                   const int32_t *seq_lens, int top_k, int32_t *idx_out, void *out,
+                   float *out_f32, float *scores_out, cudaStream_t st)
+{
+    const bool select = top_k > 0;
+    td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
+    a.scores = select ? (scores_out ? scores_out : (float *)(c.wsb + c.ws.scores)) : nullptr;
+    plan_splits(c.shape, c.shape.max_seq_len, false, select, a.nsplit, a.chunk);
+    if (td::launch_attention(c.G, false, select, a, c.shape.batch, st) != cudaSuccess)
+        return TD_ERR_CUDA;
+    if (select) {
+        td::TopkArgs t{};
+        t.scores = a.scores;
+        t.seq_lens = seq_lens;
+        t.idx = idx_out;
+        t.status = a.status;
+        t.Hkv = c.shape.num_kv_heads;
+        t.Nmax = c.shape.max_seq_len;
+        t.top_k = top_k;
+        if (td::launch_topk(t, c.shape.batch, st) != cudaSuccess)
+            return TD_ERR_CUDA;
+    }
+    return TD_OK;
+}
+
+td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
+                     const int32_t *seq_lens, const int32_t *idx, int top_k, void *out,
+                     float *out_f32, cudaStream_t st)
+{
+    td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
+    a.idx = idx;
+    a.top_k = top_k;
+    plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
+    if (td::launch_attention(c.G, true, false, a, c.shape.batch, st) != cudaSuccess)
+        return TD_ERR_CUDA;
+    return TD_OK;
+}
+
+td_status validate_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
+                        const void *const *q, const void *const *k_caches,
+                        const void *const *v_caches, const int32_t *seq_lens, int32_t top_k,
+                        const int32_t *idx_buf, int32_t idx_valid, void *const *outs,
+                        float *const *outs_f32)
+{
+    (void)c;
+    if (num_layers < 0 || (num_layers > 0 && (!modes || !q || !k_caches || !v_caches || !outs)))
+        return TD_ERR_INVALID_ARG;
+    if (!seq_lens || !aligned(seq_lens, 4))
+        return TD_ERR_INVALID_ARG;
+    bool have_set = idx_valid != 0;
+    bool uses_idx = false;
+    for (int l = 0; l < num_layers; ++l) {
+        const int m = modes[l];
+        if (m != TD_MODE_FULL && m != TD_MODE_FULL_SELECT && m != TD_MODE_SPARSE)
+            return TD_ERR_INVALID_ARG;
+        td_status st = check_layer_ptrs(q[l], k_caches[l], v_caches[l], outs[l],
+                                        outs_f32 ? outs_f32[l] : nullptr);
+        if (st)
+            return st;
+        if (m == TD_MODE_FULL_SELECT) {
+            if (top_k < 1)
+                return TD_ERR_INVALID_ARG;
+            have_set = true;
+            uses_idx = true;
+        } else if (m == TD_MODE_SPARSE) {
+            if (top_k < 1)
+                return TD_ERR_INVALID_ARG;
+            if (!have_set)
+                return TD_ERR_NO_SELECTION;
+            uses_idx = true;
+        }
+    }
+    if (uses_idx && (!idx_buf || !aligned(idx_buf, 4)))
+        return TD_ERR_INVALID_ARG;
+    return TD_OK;
+}
+
+td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
+                       const void *const *q, const void *const *k_caches,
+                       const void *const *v_caches, const int32_t *seq_lens, int32_t top_k,
+                       int32_t *idx_buf, void *const *outs, float *const *outs_f32,
+                       cudaStream_t st, void *const *layer_events)
+{
+    for (int l = 0; l < num_layers; ++l) {
+        if (layer_events && layer_events[l] &&
+            cudaEventRecord((cudaEvent_t)layer_events[l], st) != cudaSuccess)
+            return TD_ERR_CUDA;
+        float *of = outs_f32 ? outs_f32[l] : nullptr;
+        td_status r;
+        switch (modes[l]) {
+        case TD_MODE_FULL:
+            r = run_full(c, q[l], k_caches[l], v_caches[l], seq_lens, 0, nullptr, outs[l], of,
+                         nullptr, st);
+            break;
+        case TD_MODE_FULL_SELECT:
+            r = run_full(c, q[l], k_caches[l], v_caches[l], seq_lens, top_k, idx_buf, outs[l],
+                         of, nullptr, st);
+            break;
+        default:
+            r = run_sparse(c, q[l], k_caches[l], v_caches[l], seq_lens, idx_buf, top_k, outs[l],
+                           of, st);
+            break;
+        }
+        if (r)
+            return r;
+    }
+    if (layer_events && layer_events[num_layers] &&
+        cudaEventRecord((cudaEvent_t)layer_events[num_layers], st) != cudaSuccess)
+        return TD_ERR_CUDA;
+    return TD_OK;
+}
+
+}  // namespace
+
+struct td_plan {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" {
+
+const char *td_status_string(td_status status)
+{
+    switch (status) {
+    case TD_OK: return "TD_OK";
+    case TD_ERR_INVALID_ARG: return "TD_ERR_INVALID_ARG";
+    case TD_ERR_UNSUPPORTED_SHAPE: return "TD_ERR_UNSUPPORTED_SHAPE";
+    case TD_ERR_NO_SELECTION: return "TD_ERR_NO_SELECTION";
+    case TD_ERR_WORKSPACE_TOO_SMALL: return "TD_ERR_WORKSPACE_TOO_SMALL";
+    case TD_ERR_CUDA: return "TD_ERR_CUDA";
+    }
+    return "TD_ERR_UNKNOWN";
+}
+
+size_t td_workspace_size(const td_shape *shape, int32_t top_k)
+{
+    if (check_shape(shape) != TD_OK || top_k < 0 || top_k > shape->max_seq_len ||
+        top_k > td::kMaxTopK)
+        return 0;
+    return ws_layout(*shape, top_k).total;
+}
+
+td_status td_workspace_init(void *ws, size_t ws_bytes, void *stream)
+{
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < kAlign)
+        return TD_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream) != cudaSuccess)
+        return TD_ERR_CUDA;
+    return TD_OK;
+}
+
+td_status td_workspace_status(void *ws, size_t ws_bytes, uint32_t *flags, void *stream)
+{
+    if (!ws || !flags || !aligned(ws, kAlign) || ws_bytes < kAlign)
+        return TD_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint32_t host = 0;
+    if (cudaMemcpyAsync(&host, ws, sizeof host, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return TD_ERR_CUDA;
+    *flags = host;
+    return TD_OK;
+}
+
+td_status td_full_attn_select(const td_shape *shape, const void *q, const void *k_cache,
+                              const void *v_cache, const int32_t *seq_lens, int32_t top_k,
+                              int32_t *idx_out, void *out, float *out_f32, float *scores_out,
+                              void *ws, size_t ws_bytes, void *stream)
+{
+    Ctx c;
+    td_status st = make_ctx(shape, top_k, ws, ws_bytes, c);
+    if (st)
+        return st;
+    st = check_layer_ptrs(q, k_cache, v_cache, out, out_f32);
+    if (st)
+        return st;
+    if (!seq_lens || !aligned(seq_lens, 4))
+        return TD_ERR_INVALID_ARG;
+    if (top_k > 0 && (!idx_out || !aligned(idx_out, 4)))
+        return TD_ERR_INVALID_ARG;
+    if (scores_out && !aligned(scores_out, 4))
+        return TD_ERR_INVALID_ARG;
+    return run_full(c, q, k_cache, v_cache, seq_lens, top_k, idx_out, out, out_f32,
+                    top_k > 0 ? scores_out : nullptr, (cudaStream_t)stream);
+}
+
+td_status td_topk_select(const td_shape *shape, const float *scores, const int32_t *seq_lens,
+                         int32_t top_k, int32_t *idx_out, void *ws, size_t ws_bytes,
+                         void *stream)
+{
+    Ctx c;
+    td_status st = make_ctx(shape, top_k, ws, ws_bytes, c);
+    if (st)
+        return st;
+    if (top_k < 1 || !scores || !aligned(scores, 4) || !seq_lens || !aligned(seq_lens, 4) ||
+        !idx_out || !aligned(idx_out, 4))
+        return TD_ERR_INVALID_ARG;
+    td::TopkArgs t{};
+    t.scores = scores;
+    t.seq_lens = seq_lens;
+    t.idx = idx_out;
+    t.status = (uint32_t *)(c.wsb + c.ws.status);
+    t.Hkv = c.shape.num_kv_heads;
+    t.Nmax = c.shape.max_seq_len;
+    t.top_k = top_k;
+    if (td::launch_topk(t, c.shape.batch, (cudaStream_t)stream) != cudaSuccess)
+        return TD_ERR_CUDA;
+    return TD_OK;
+}
+
+td_status td_sparse_attn(const td_shape *shape, const void *q, const void *k_cache,
+                         const void *v_cache, const int32_t *seq_lens, const int32_t *idx,
+                         int32_t top_k, void *out, float *out_f32, void *ws, size_t ws_bytes,
+                         void *stream)
+{
+    Ctx c;
+    td_status st = make_ctx(shape, top_k, ws, ws_bytes, c);
+    if (st)
+        return st;
+    st = check_layer_ptrs(q, k_cache, v_cache, out, out_f32);
+    if (st)
+        return st;
+    if (top_k < 1 || !idx || !aligned(idx, 4) || !seq_lens || !aligned(seq_lens, 4))
+        return TD_ERR_INVALID_ARG;
+    return run_sparse(c, q, k_cache, v_cache, seq_lens, idx, top_k, out, out_f32,
+                      (cudaStream_t)stream);
+}
+
+td_status td_decode_step(const td_shape *shape, int32_t num_layers, const int32_t *modes,
+                         const void *const *q, const void *const *k_caches,
+                         const void *const *v_caches, const int32_t *seq_lens, int32_t top_k,
+                         int32_t *idx_buf, int32_t idx_valid, void *const *outs,
+                         float *const *outs_f32, void *ws, size_t ws_bytes, void *stream,
+                         void *const *layer_events)
+{
+    Ctx c;
+    td_status st = make_ctx(shape, top_k, ws, ws_bytes, c);
+    if (st)
+        return st;
+    st = validate_step(c, num_layers, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf,
+                       idx_valid, outs, outs_f32);
+    if (st)
+        return st;
+    return enqueue_step(c, num_layers, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf,
+                        outs, outs_f32, (cudaStream_t)stream, layer_events);
+}
+
+td_status td_plan_create(td_plan **plan, const td_shape *shape, int32_t num_layers,
+                         const int32_t *modes, const void *const *q,
+                         const void *const *k_caches, const void *const *v_caches,
+                         const int32_t *seq_lens, int32_t top_k, int32_t *idx_buf,
+                         int32_t idx_valid, void *const *outs, float *const *outs_f32, void *ws,
+                         size_t ws_bytes)
+{
+    if (!plan)
+        return TD_ERR_INVALID_ARG;
+    *plan = nullptr;
+    Ctx c;
+    td_status st = make_ctx(shape, top_k, ws, ws_bytes, c);
+    if (st)
+        return st;
+    st = validate_step(c, num_layers, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf,
+                       idx_valid, outs, outs_f32);
+    if (st)
+        return st;
+    td_plan *p = new (std::nothrow) td_plan();
+    if (!p)
+        return TD_ERR_INVALID_ARG;
+    cudaStream_t cap = nullptr;
+    if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) {
+        delete p;
+        return TD_ERR_CUDA;
+    }
+    st = TD_OK;
+    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        st = TD_ERR_CUDA;
+    } else {
+        td_status enq = enqueue_step(c, num_layers, modes, q, k_caches, v_caches, seq_lens,
+                                     top_k, idx_buf, outs, outs_f32, cap, nullptr);
+        cudaGraph_t graph = nullptr;
+        const cudaError_t end = cudaStreamEndCapture(cap, &graph);
+        if (enq != TD_OK || end != cudaSuccess) {
+            st = enq != TD_OK ? enq : TD_ERR_CUDA;
+            if (graph)
+                cudaGraphDestroy(graph);
+        } else {
+            p->graph = graph;
+            if (cudaGraphInstantiate(&p->exec, graph, 0) != cudaSuccess)
+                st = TD_ERR_CUDA;
+        }
+    }
+    cudaStreamDestroy(cap);
+    if (st) {
+        td_plan_destroy(p);
+        return st;
+    }
+    *plan = p;
+    return TD_OK;
+}
+
+td_status td_plan_launch(td_plan *plan, void *stream)
+{
+    if (!plan || !plan->exec)
+        return TD_ERR_INVALID_ARG;
+    if (cudaGraphLaunch(plan->exec, (cudaStream_t)stream) != cudaSuccess)
+        return TD_ERR_CUDA;
+    return TD_OK;
+}
+
+void td_plan_destroy(td_plan *plan)
+{
+    if (!plan)
+        return;
+    if (plan->exec)
+        cudaGraphExecDestroy(plan->exec);
+    if (plan->graph)
+        cudaGraphDestroy(plan->graph);
+    delete plan;
+}
+
+td_status td_set_tuning(const char *key, int32_t value)
+{
+    if (!key)
+        return TD_ERR_INVALID_ARG;
+    if (!strcmp(key, "full_ctas_per_sm"))
+        g_tuning.full_ctas_per_sm = value > 0 ? value : kDefaultTuning.full_ctas_per_sm;
+    else if (!strcmp(key, "sparse_ctas_per_sm"))
+        g_tuning.sparse_ctas_per_sm = value > 0 ? value : kDefaultTuning.sparse_ctas_per_sm;
+    else if (!strcmp(key, "full_waves"))
+        g_tuning.full_waves = value > 0 ? value : kDefaultTuning.full_waves;
+    else if (!strcmp(key, "sparse_waves"))
+        g_tuning.sparse_waves = value > 0 ? value : kDefaultTuning.sparse_waves;
+    else if (!strcmp(key, "max_splits"))
+        g_tuning.max_splits = (value > 0 && value <= td::kMaxSplits) ? value : td::kMaxSplits;
+    else
+        return TD_ERR_INVALID_ARG;
+    return TD_OK;
+}
+
+int32_t td_query_splits(const td_shape *shape, int32_t top_k, int32_t sparse)
+{
+    if (check_shape(shape) != TD_OK)
+        return 0;
+    int nsplit = 0, chunk = 0;
+    plan_splits(*shape, sparse ? top_k : shape->max_seq_len, sparse != 0, !sparse && top_k > 0,
+                nsplit, chunk);
+    return nsplit;
+}
+
+}  // extern "C"

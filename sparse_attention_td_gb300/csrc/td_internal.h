@@ -1,0 +1,63 @@
+// td_internal.h -- kernel arguments and launchers shared by the library's
+// translation units (not part of the public C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace td {
+
+constexpr int kHeadDim = 128;          // only head_dim supported
+constexpr int kAttnThreads = 256;      // 8 warps
+constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kTokPerHalf = 4;         // tokens a half-warp holds in flight per round
+constexpr int kTokPerRound = kAttnWarps * 2 * kTokPerHalf;  // 64 tokens per CTA round
+constexpr int kMaxSplits = 256;        // splits per (batch, KV head)
+constexpr int kMaxSplitCtas = 8192;    // cap on batch * kv_heads * splits for partials
+constexpr int kMaxSparseChunk = 2048;  // index entries one sparse CTA stages in shared memory
+constexpr int kMaxTopK = kMaxSplits * kMaxSparseChunk;
+constexpr int kTopkThreads = 1024;
+
+constexpr uint32_t kFlagIndexOutOfRange = 0x1u;
+constexpr uint32_t kFlagSeqLenOutOfRange = 0x2u;
+
+// One attention launch (full or sparse).  Partials are struct-of-arrays over
+// (batch*kv_head, split, head-in-group[, dim]) with split stride `nsplit`.
+struct AttnArgs {
+    const uint16_t *q;       // [B][Hq][128] bf16 bits
+    const uint16_t *k;       // [B][Hkv][Nmax][128]
+    const uint16_t *v;
+    const int32_t *seq_lens; // [B]
+    const int32_t *idx;      // sparse: [B][Hkv][top_k]
+    uint16_t *out;           // [B][Hq][128]
+    float *out_f32;          // optional
+    float *scores;           // select: [B][Hkv][Nmax]
+    float *part_m;           // [B*Hkv][nsplit][G]  running max (log2 units)
+    float *part_l;           // [B*Hkv][nsplit][G]  softmax denominator
+    float *part_o;           // [B*Hkv][nsplit][G][128] un-normalised output
+    uint32_t *tickets;       // [B*Hkv] arrival counters, zero between launches
+    uint32_t *status;        // device status word
+    int Hq, Hkv, Nmax, top_k;
+    int chunk;               // tokens (full) or index entries (sparse) per split
+    int nsplit;              // gridDim.x
+    float scale;             // softmax scale (natural-log units)
+};
+
+struct TopkArgs {
+    const float *scores;     // [B][Hkv][Nmax]
+    const int32_t *seq_lens; // [B]
+    int32_t *idx;            // [B][Hkv][top_k]
+    uint32_t *status;
+    int Hkv, Nmax, top_k;
+};
+
+// G = query heads per KV head (1, 2, 4, 8).
+cudaError_t launch_attention(int G, bool sparse, bool select, const AttnArgs &a, int batch,
+                             cudaStream_t stream);
+cudaError_t launch_topk(const TopkArgs &a, int batch, cudaStream_t stream);
+
+// Resident CTAs per SM of one attention instantiation (occupancy query).
+int attention_ctas_per_sm(int G, bool sparse, bool select);
+
+}  // namespace td

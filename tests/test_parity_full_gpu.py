@@ -1,0 +1,100 @@
+"""Full-size workloads: the decode step exactly as the bench launches it (a
+captured CUDA-graph plan), compared with the oracle on sampled (batch row,
+KV head) groups through every layer of the schedule.
+
+Each sampled group is independent of the others (its sparse layers read only
+its own persisted set), so the oracle runs the group's whole schedule on
+host copies of that group's q/K/V slices.  Selected sets are compared under
+the tie rule; sparse layers downstream of a set that differs by a tolerated
+swap are not compared (they attend over a different, equally valid set).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_td_gb300 as td
+import workloads as W
+from parity_util import check_index_set, check_outputs
+
+pytestmark = pytest.mark.gpu
+
+CASES = [("llama2-7b-10k", None, 4), ("llama3-8b-32k", None, 4), ("llama2-7b-100k", None, 3),
+         ("serving-b32", 256, 4), ("serving-b32", 1024, 4), ("serving-b32", 4096, 4)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _groups(wl, lens, n):
+    rs = np.random.RandomState(wl.seed + 77)
+    picks = {(int(np.argmin(lens)), 0), (int(np.argmax(lens)), wl.kv_heads - 1)}
+    while len(picks) < n:
+        picks.add((int(rs.randint(wl.batch)), int(rs.randint(wl.kv_heads))))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name,k,n_groups", CASES, ids=[f"{c[0]}-k{c[1]}" for c in CASES])
+def test_full_size_step_sampled(name, k, n_groups):
+    wl = W.WORKLOADS[name]
+    if k is not None:
+        wl = wl.with_(top_k=k)
+    G, D = wl.group, wl.head_dim
+    heavy = W.heavy_positions(wl)
+    lens = W.seq_lens(wl)
+    layers = [W.generate_layer(wl, layer, "cuda", heavy[layer]) for layer in range(wl.layers)]
+    q = [x[0] for x in layers]
+    K = [x[1] for x in layers]
+    V = [x[2] for x in layers]
+    del layers
+    seq = torch.as_tensor(lens).cuda()
+    scale = td.default_scale(D)
+    shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len, scale=scale)
+    outs = [torch.empty_like(x) for x in q]
+    outs32 = [torch.empty(x.shape, dtype=torch.float32, device="cuda") for x in q]
+    idx = torch.full((wl.batch, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device="cuda")
+    ws = td.Workspace(shape, wl.top_k)
+    sel_layers = [i for i, m in enumerate(wl.modes) if m == W.FULL_SELECT]
+    first, middle = sel_layers[0], sel_layers[-1]
+
+    # the first selection's set, from the schedule's prefix
+    td.td_decode_step(shape, wl.modes[:middle], q[:middle], K[:middle], V[:middle], seq,
+                      wl.top_k, idx, outs[:middle], outs32[:middle], ws)
+    torch.cuda.synchronize()
+    idx_first = idx.cpu().numpy()
+    # the whole step, as the bench runs it
+    plan = td.Plan(shape, wl.modes, q, K, V, seq, wl.top_k, idx, outs, outs32, ws)
+    plan.launch()
+    torch.cuda.synchronize()
+    plan.close()
+    assert ws.status() == 0
+    idx_final = idx.cpu().numpy()
+
+    orc = oracle.get()
+    compared = 0
+    for b, g in _groups(wl, lens, n_groups):
+        n = int(lens[b])
+        qg = [W.u16(x[b, g * G:(g + 1) * G]) for x in q]
+        Kg = [W.u16(x[b, g, :n]) for x in K]
+        Vg = [W.u16(x[b, g, :n]) for x in V]
+        ref, per_layer, final, rc = orc.decode_group(list(wl.modes), qg, Kg, Vg, n, wl.top_k,
+                                                     scale)
+        assert rc == 0
+        s1 = orc.group_scores(qg[first], Kg[first], n, scale)
+        s2 = orc.group_scores(qg[middle], Kg[middle], n, scale)
+        ok1 = check_index_set(idx_first[b, g], per_layer[first], s1, wl.top_k, f"L{first} b{b}g{g}")
+        ok2 = check_index_set(idx_final[b, g], per_layer[middle], s2, wl.top_k,
+                              f"L{middle} b{b}g{g}")
+        for layer, mode in enumerate(wl.modes):
+            if mode == W.SPARSE and not (ok1 if layer < middle else ok2):
+                continue
+            check_outputs(outs[layer][b, g * G:(g + 1) * G], outs32[layer][b, g * G:(g + 1) * G],
+                          ref[layer], f"{name} L{layer} b{b} g{g}")
+            compared += 1
+    assert compared >= n_groups * (wl.layers - 8)
+    del q, K, V, outs, outs32
+    torch.cuda.empty_cache()

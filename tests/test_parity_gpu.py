@@ -1,0 +1,335 @@
+"""CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Small cases span several splits and ragged tails and are compared element by
+element; degenerate cases (empty context, k >= N, padding, ties) are covered
+explicitly.  The full-size workloads live in test_parity_full_gpu.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_td_gb300 as td
+import workloads as W
+from parity_util import check_index_set, check_outputs
+
+pytestmark = pytest.mark.gpu
+D = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    td.td_set_tuning("max_splits", 0)
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+def _dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+def run_full(shape, q, K, V, lens, top_k=0):
+    B, Hq, Hkv = shape.batch, shape.num_q_heads, shape.num_kv_heads
+    qd, Kd, Vd = _dev(q, K, V)
+    seq = torch.as_tensor(np.asarray(lens, np.int32)).cuda()
+    out = torch.empty_like(qd)
+    out32 = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
+    idx = torch.full((B, Hkv, max(top_k, 1)), -7, dtype=torch.int32, device="cuda")
+    scores = torch.full((B, Hkv, shape.max_seq_len), float("nan"), device="cuda")
+    ws = td.Workspace(shape, top_k)
+    td.td_full_attn_select(shape, qd, Kd, Vd, seq, top_k, idx if top_k else None, out, out32,
+                           scores if top_k else None, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    return out, out32, idx[..., :top_k].cpu().numpy(), scores.cpu().numpy()
+
+
+def oracle_full(orc, shape, q, K, V, lens):
+    B, Hq, Hkv = shape.batch, shape.num_q_heads, shape.num_kv_heads
+    G = Hq // Hkv
+    qb, Kb, Vb = W.u16(q), W.u16(K), W.u16(V)
+    ref = np.zeros((B, Hq, D))
+    for b in range(B):
+        for h in range(Hq):
+            ref[b, h] = orc.attend(qb[b, h], Kb[b, h // G, :lens[b]], Vb[b, h // G, :lens[b]],
+                                   shape.scale)
+    return ref
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("max_splits", [0, 1])
+def test_full_attention_ragged(orc, G, max_splits):
+    td.td_set_tuning("max_splits", max_splits)
+    Hkv, B, N = 2, 4, 700
+    lens = [700, 0, 333, 45]            # full, empty, ragged tail, shorter than one round
+    shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
+    q, K, V, _ = W.random_case(10 + G, B, G * Hkv, Hkv, N, lens)
+    out, out32, _, _ = run_full(shape, q, K, V, lens)
+    ref = oracle_full(orc, shape, q, K, V, lens)
+    check_outputs(out, out32, ref, f"G={G}")
+    assert torch.all(out[1] == 0) and torch.all(out32[1] == 0)   # empty context -> 0
+    td.td_set_tuning("max_splits", 0)
+
+
+def test_full_attention_planted_large_logits(orc):
+    """Sink-like keys (x3) and planted directions give logits up to ~30."""
+    wl = W.WORKLOADS["llama2-7b-100k"].with_(batch=1, layers=1, q_heads=4, kv_heads=4,
+                                             max_seq_len=3000, heavy=64, top_k=128)
+    q, K, V = W.generate_layer(wl, 0)
+    shape = td.make_shape(1, 4, 4, 3000, scale=td.default_scale(D))
+    out, out32, _, _ = run_full(shape, q, K, V, [3000])
+    check_outputs(out, out32, oracle_full(orc, shape, q, K, V, [3000]), "planted")
+
+
+@pytest.mark.parametrize("G,k", [(1, 64), (4, 100), (8, 256), (2, 1)])
+def test_full_select_scores_and_sets(orc, G, k):
+    Hkv, B, N = 2, 3, 1500
+    lens = [1500, 777, 50]              # the last row has fewer tokens than k for k >= 64
+    shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
+    q, K, V, _ = W.random_case(20 + G, B, G * Hkv, Hkv, N, lens)
+    out, out32, idx, scores = run_full(shape, q, K, V, lens, top_k=k)
+    check_outputs(out, out32, oracle_full(orc, shape, q, K, V, lens), "select outputs")
+    qb, Kb = W.u16(q), W.u16(K)
+    exact = 0
+    for b in range(B):
+        for g in range(Hkv):
+            s_ref = orc.group_scores(qb[b, g * G:(g + 1) * G], Kb[b, g], lens[b], shape.scale)
+            s_got = scores[b, g, :lens[b]].astype(np.float64)
+            assert np.allclose(s_got, s_ref, rtol=1e-5, atol=1e-4), "emitted scores off"
+            assert np.all(np.isnan(scores[b, g, lens[b]:]))      # nothing written past N_b
+            ref_idx = orc.topk(s_ref, k)
+            exact += check_index_set(idx[b, g], ref_idx, s_ref, k, f"b{b} g{g}")
+    assert exact >= B * Hkv - 1
+
+
+def _topk_case(scores_rows, lens, k):
+    """Run td_topk_select on explicit fp32 score rows ([B][1][Nmax])."""
+    B = len(scores_rows)
+    N = max(len(r) for r in scores_rows)
+    arr = np.full((B, 1, N), 7.0, dtype=np.float32)
+    for b, r in enumerate(scores_rows):
+        arr[b, 0, :len(r)] = r
+    shape = td.make_shape(B, 1, 1, N)
+    sc = torch.as_tensor(arr).cuda()
+    seq = torch.as_tensor(np.asarray(lens, np.int32)).cuda()
+    idx = torch.full((B, 1, k), -9, dtype=torch.int32, device="cuda")
+    ws = td.Workspace(shape, k)
+    td.td_topk_select(shape, sc, seq, k, idx, ws)
+    torch.cuda.synchronize()
+    return arr, idx.cpu().numpy()
+
+
+def test_topk_adversarial(orc):
+    rs = np.random.RandomState(5)
+    N = 5000
+    rows = [
+        rs.randn(N).astype(np.float32),                                  # random
+        np.zeros(N, np.float32),                                         # all equal
+        np.round(rs.randn(N) * 2).astype(np.float32),                    # many ties at the k-th
+        np.where(rs.rand(N) < 0.5, -0.0, 0.0).astype(np.float32),        # +-0 only
+        -np.abs(rs.randn(N)).astype(np.float32),                         # negative only
+        np.concatenate([np.full(10, 3.0), np.full(N - 10, -1.0)]).astype(np.float32),
+        np.array([np.inf, -np.inf, 1.0, -1.0] * (N // 4), np.float32),   # infinities
+        rs.randn(N).astype(np.float32),                                  # N_b < k (lens 40)
+        rs.randn(N).astype(np.float32),                                  # N_b = 0
+        (rs.randint(0, 3, N) * 1e-39).astype(np.float32),                # subnormal ties
+    ]
+    lens = [N] * 7 + [40, 0, N]
+    for k in (1, 64, 300, N):
+        arr, got = _topk_case(rows, lens, k)
+        for b in range(len(rows)):
+            want = orc.topk(arr[b, 0, :lens[b]].astype(np.float64), k)
+            assert np.array_equal(got[b, 0], want), f"row {b} k={k}"
+
+
+def test_topk_large_rows(orc):
+    rs = np.random.RandomState(6)
+    N, k = 102400, 4096
+    rows = [np.round(rs.randn(N) * 50).astype(np.float32) for _ in range(3)]
+    lens = [N, N - 1, 65537]
+    arr, got = _topk_case(rows, lens, k)
+    for b in range(3):
+        want = orc.topk(arr[b, 0, :lens[b]].astype(np.float64), k)
+        assert np.array_equal(got[b, 0], want), f"row {b}"
+
+
+def run_sparse(shape, q, K, V, lens, idx_np, top_k):
+    qd, Kd, Vd = _dev(q, K, V)
+    seq = torch.as_tensor(np.asarray(lens, np.int32)).cuda()
+    idx = torch.as_tensor(idx_np.astype(np.int32)).cuda()
+    out = torch.empty_like(qd)
+    out32 = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
+    ws = td.Workspace(shape, top_k)
+    td.td_sparse_attn(shape, qd, Kd, Vd, seq, idx, top_k, out, out32, ws)
+    torch.cuda.synchronize()
+    return out, out32, ws.status()
+
+
+def oracle_sparse(orc, shape, q, K, V, idx_np):
+    B, Hq, Hkv = shape.batch, shape.num_q_heads, shape.num_kv_heads
+    G = Hq // Hkv
+    qb, Kb, Vb = W.u16(q), W.u16(K), W.u16(V)
+    ref = np.zeros((B, Hq, D))
+    for b in range(B):
+        for h in range(Hq):
+            rows = idx_np[b, h // G]
+            rows = rows[rows >= 0]
+            ref[b, h] = orc.attend(qb[b, h], Kb[b, h // G], Vb[b, h // G], shape.scale, rows=rows)
+    return ref
+
+
+@pytest.mark.parametrize("G,k", [(1, 300), (4, 64), (8, 1000), (2, 1)])
+def test_sparse_random_sets(orc, G, k):
+    Hkv, B, N = 2, 3, 2000
+    lens = [2000, 1200, 500]
+    shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
+    q, K, V, _ = W.random_case(30 + G, B, G * Hkv, Hkv, N, lens)
+    idx = W.random_index_sets(31 + G, B, Hkv, k, lens, pad_fraction=0.1 if k > 1 else 0.0)
+    rs = np.random.RandomState(32)
+    for row in idx.reshape(-1, k):             # order inside a set must not matter
+        rs.shuffle(row)
+    out, out32, status = run_sparse(shape, q, K, V, lens, idx, k)
+    assert status == 0
+    check_outputs(out, out32, oracle_sparse(orc, shape, q, K, V, idx), f"sparse G={G} k={k}")
+
+
+def test_sparse_all_padding_and_all_positions(orc):
+    G, Hkv, B, N = 4, 2, 2, 640
+    lens = [640, 640]
+    shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
+    q, K, V, _ = W.random_case(40, B, G * Hkv, Hkv, N, lens)
+    idx = np.full((B, Hkv, N), -1, np.int32)
+    idx[0] = np.arange(N)                      # k = N: every position
+    out, out32, status = run_sparse(shape, q, K, V, lens, idx, N)
+    assert status == 0
+    assert torch.all(out[1] == 0)              # all padding -> 0
+    fo, fo32, _, _ = run_full(shape, q, K, V, lens)
+    ref = oracle_full(orc, shape, q, K, V, lens)
+    check_outputs(out[:1], out32[:1], ref[:1], "k=N sparse")
+    # sparse over every position equals full attention (fp32, different split order)
+    assert torch.allclose(out32[0], fo32[0], rtol=0, atol=1e-5 * float(fo32[0].abs().max()))
+
+
+def test_sparse_bad_index_is_flagged_and_skipped(orc):
+    G, Hkv, B, N = 1, 1, 1, 256
+    shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
+    q, K, V, _ = W.random_case(41, B, 1, 1, N, [200])
+    good = np.array([[[3, 50, 199, -1]]], np.int32)
+    bad = np.array([[[3, 50, 199, 200]]], np.int32)     # 200 >= seq_lens[0]
+    out_g, out32_g, st_g = run_sparse(shape, q, K, V, [200], good, 4)
+    out_b, out32_b, st_b = run_sparse(shape, q, K, V, [200], bad, 4)
+    assert st_g == 0 and st_b == td.FLAG_INDEX_OUT_OF_RANGE
+    assert torch.equal(out32_g, out32_b)
+
+
+def test_seq_len_out_of_range_is_flagged(orc):
+    shape = td.make_shape(1, 2, 2, 128, scale=td.default_scale(D))
+    q, K, V, _ = W.random_case(42, 1, 2, 2, 128, [128])
+    qd, Kd, Vd = _dev(q, K, V)
+    seq = torch.tensor([500], dtype=torch.int32, device="cuda")      # > max_seq_len
+    out = torch.empty_like(qd)
+    out32 = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
+    ws = td.Workspace(shape, 0)
+    td.td_full_attn_select(shape, qd, Kd, Vd, seq, 0, None, out, out32, None, ws)
+    assert ws.status() == td.FLAG_SEQ_LEN_OUT_OF_RANGE
+    check_outputs(out, out32, oracle_full(orc, shape, q, K, V, [128]), "clamped")
+
+
+def _tiny_inputs():
+    wl = W.WORKLOADS["tiny"]
+    heavy = W.heavy_positions(wl)
+    layers = [W.generate_layer(wl, layer, "cpu", heavy[layer]) for layer in range(wl.layers)]
+    return wl, layers
+
+
+def test_decode_step_tiny_matches_oracle(orc):
+    wl, layers = _tiny_inputs()
+    lens = W.seq_lens(wl)
+    shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len,
+                          scale=td.default_scale(D))
+    q = [x[0].cuda() for x in layers]
+    K = [x[1].cuda() for x in layers]
+    V = [x[2].cuda() for x in layers]
+    outs = [torch.empty_like(x) for x in q]
+    outs32 = [torch.empty(x.shape, dtype=torch.float32, device="cuda") for x in q]
+    idx = torch.full((1, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device="cuda")
+    ws = td.Workspace(shape, wl.top_k)
+    td.td_decode_step(shape, wl.modes, q, K, V, torch.as_tensor(lens).cuda(), wl.top_k, idx,
+                      outs, outs32, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    ref, ref_idx, rc = orc.decode_step(list(wl.modes), [W.u16(x[0]) for x in layers],
+                                       [W.u16(x[1]) for x in layers],
+                                       [W.u16(x[2]) for x in layers], lens, wl.top_k, shape.scale)
+    assert rc == 0
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    for layer in range(wl.layers):
+        check_outputs(outs[layer], outs32[layer], ref[layer], f"layer {layer}")
+
+
+def test_plan_replays_the_step_bitwise():
+    wl, layers = _tiny_inputs()
+    shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len)
+    q = [x[0].cuda() for x in layers]
+    K = [x[1].cuda() for x in layers]
+    V = [x[2].cuda() for x in layers]
+    seq = torch.as_tensor(W.seq_lens(wl)).cuda()
+    res = []
+    for use_plan in (False, True):
+        outs = [torch.zeros_like(x) for x in q]
+        outs32 = [torch.zeros(x.shape, dtype=torch.float32, device="cuda") for x in q]
+        idx = torch.full((1, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device="cuda")
+        ws = td.Workspace(shape, wl.top_k)
+        if use_plan:
+            plan = td.Plan(shape, wl.modes, q, K, V, seq, wl.top_k, idx, outs, outs32, ws)
+            plan.launch()
+            plan.launch()                   # replays leave the workspace reusable
+            plan.close()
+        else:
+            td.td_decode_step(shape, wl.modes, q, K, V, seq, wl.top_k, idx, outs, outs32, ws)
+        torch.cuda.synchronize()
+        res.append((idx.clone(), [o.clone() for o in outs32]))
+    assert torch.equal(res[0][0], res[1][0])
+    for a, b in zip(res[0][1], res[1][1]):
+        assert torch.equal(a, b)
+
+
+def test_layer_events_time_each_layer():
+    wl, layers = _tiny_inputs()
+    shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len)
+    q = [x[0].cuda() for x in layers]
+    K = [x[1].cuda() for x in layers]
+    V = [x[2].cuda() for x in layers]
+    outs = [torch.empty_like(x) for x in q]
+    idx = torch.full((1, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device="cuda")
+    ws = td.Workspace(shape, wl.top_k)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(wl.layers + 1)]
+    td.td_decode_step(shape, wl.modes, q, K, V, torch.as_tensor(W.seq_lens(wl)).cuda(),
+                      wl.top_k, idx, outs, None, ws, layer_events=ev)
+    torch.cuda.synchronize()
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(wl.layers)]
+    assert all(t > 0 for t in times)
+
+
+def test_sparse_before_selection_launches_nothing():
+    shape = td.make_shape(1, 2, 2, 64)
+    x = torch.zeros(1, 2, D, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(1, 2, 64, D, dtype=torch.bfloat16, device="cuda")
+    seq = torch.tensor([64], dtype=torch.int32, device="cuda")
+    idx = torch.zeros(1, 2, 4, dtype=torch.int32, device="cuda")
+    ws = td.Workspace(shape, 4)
+    with pytest.raises(td.TdError) as e:
+        td.td_decode_step(shape, [td.MODE_FULL, td.MODE_SPARSE], [x, x], [kv, kv], [kv, kv], seq,
+                          4, idx, [x, x], None, ws)
+    assert e.value.status == 3
+    # with a caller-provided set the same schedule is accepted
+    td.td_decode_step(shape, [td.MODE_FULL, td.MODE_SPARSE], [x, x], [kv, kv], [kv, kv], seq, 4,
+                      idx, [x.clone(), x.clone()], None, ws, idx_valid=True)
+    torch.cuda.synchronize()
