@@ -156,37 +156,39 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- oracle timing
-def oracle_sample(wl: W.Workload, host_layers, lens, n_groups: int, modes):
-    """Time the CPU oracle on n_groups sampled (batch row, KV head) groups over
-    all layers; returns (seconds for the sample, groups timed, threads)."""
-    import oracle
-    orc = oracle.get()
-    G = wl.group
+def pick_groups(wl: W.Workload, n_groups: int):
     rs = np.random.RandomState(wl.seed + 5)
     all_groups = [(b, g) for b in range(wl.batch) for g in range(wl.kv_heads)]
-    pick = [all_groups[i] for i in sorted(rs.choice(len(all_groups),
-                                                    size=min(n_groups, len(all_groups)),
-                                                    replace=False))]
+    n = min(n_groups, len(all_groups))
+    return [all_groups[i] for i in sorted(rs.choice(len(all_groups), size=n, replace=False))]
+
+
+def host_sample(layers, wl: W.Workload, lens, pick):
+    """Host copies (bf16 bits) of the sampled groups' q/K/V slices, laid out as
+    a batch of len(pick) rows with one KV head each."""
+    G = wl.group
     nmax = int(max(lens[b] for b, _ in pick))
     qs, Ks, Vs = [], [], []
-    for (qh, Kh, Vh) in host_layers:
-        qs.append(np.ascontiguousarray(np.stack([qh[b, g * G:(g + 1) * G] for b, g in pick])))
-        Ks.append(np.ascontiguousarray(np.stack([Kh[b, g:g + 1, :nmax] for b, g in pick])))
-        Vs.append(np.ascontiguousarray(np.stack([Vh[b, g:g + 1, :nmax] for b, g in pick])))
-    sl = np.array([lens[b] for b, _ in pick], np.int32)
+    for q, K, V in layers:
+        qs.append(np.ascontiguousarray(np.stack([W.u16(q[b, g * G:(g + 1) * G]) for b, g in pick])))
+        Ks.append(np.ascontiguousarray(np.stack([W.u16(K[b, g:g + 1, :nmax]) for b, g in pick])))
+        Vs.append(np.ascontiguousarray(np.stack([W.u16(V[b, g:g + 1, :nmax]) for b, g in pick])))
+    return qs, Ks, Vs, np.array([lens[b] for b, _ in pick], np.int32)
+
+
+def time_oracle(wl: W.Workload, sample, modes):
+    """Seconds the CPU oracle takes for the sample through all layers, and the
+    threads it used."""
+    import oracle
+    orc = oracle.get()
+    qs, Ks, Vs, sl = sample
     scale = float(np.float32(1.0) / np.sqrt(np.float32(wl.head_dim)))
     t0 = time.perf_counter()
     _, _, rc = orc.decode_step(list(modes), qs, Ks, Vs, sl, wl.top_k, scale)
     dt = time.perf_counter() - t0
     if rc:
         raise RuntimeError(f"oracle failed: {rc}")
-    return dt, len(pick), orc.num_threads()
-
-
-def host_copies(layers, wl, n_groups):
-    """bf16 bit patterns on the host for the oracle (whole tensors; the sample
-    is cut from them)."""
-    return [(W.u16(q), W.u16(K), W.u16(V)) for q, K, V in layers]
+    return dt, orc.num_threads()
 
 
 # ----------------------------------------------------------------- helpers
@@ -402,17 +404,18 @@ def run_ours(args, world, rank, local):
             "wall_s_pass1": round(wall_ppsa, 3),
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host = host_copies(layers, wl, args.cpu_groups)
+        pick = pick_groups(wl, args.cpu_groups)
+        sample = host_sample(layers, wl, lens, pick)
         groups = wl.batch * wl.kv_heads
-        secs, n_done, threads, reps = 0.0, 0, 1, 0
+        secs, threads, reps = 0.0, 1, 0
         while secs < args.cpu_seconds and reps < 50:
-            dt, n_done, threads = oracle_sample(wl, host, lens, args.cpu_groups, modes)
+            dt, threads = time_oracle(wl, sample, modes)
             secs += dt
             reps += 1
-        per_step_us = secs / reps * (groups / n_done) * 1e6
+        per_step_us = secs / reps * (groups / len(pick)) * 1e6
         result["cpu_baseline"] = {
             "value": round(per_step_us, 1), "unit": "us", "cores": threads, "kind": "oracle",
-            "sample": f"{n_done} of {groups} (batch row, KV head) groups through all "
+            "sample": f"{len(pick)} of {groups} (batch row, KV head) groups through all "
                       f"{wl.layers} layers, x{reps} runs, scaled to the whole step",
         }
     return result
@@ -430,12 +433,14 @@ def run_reference(args, world, rank, local):
     lens = W.seq_lens(wl)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     layers = [W.generate_layer(wl, layer, dev, heavy[layer]) for layer in range(wl.layers)]
-    host = host_copies(layers, wl, args.cpu_groups)
+    pick = pick_groups(wl, args.cpu_groups)
+    sample = host_sample(layers, wl, lens, pick)
+    n_done = len(pick)
     del layers
     groups = wl.batch * wl.kv_heads
-    times, threads, n_done = [], 1, 0
+    times, threads = [], 1
     for i in range(args.warmup + args.steps):
-        dt, n_done, threads = oracle_sample(wl, host, lens, args.cpu_groups, wl.modes)
+        dt, threads = time_oracle(wl, sample, wl.modes)
         if i >= args.warmup:
             times.append(dt * (groups / n_done) * 1e6)
     value = statistics.fmean(times)
@@ -456,6 +461,59 @@ def run_reference(args, world, rank, local):
     }
 
 
+def run_profile_layer(args, local):
+    """One layer of the workload, launched alone W + K times with an L2 flush
+    before each launch: the small case for ncu captures (one layer resident)."""
+    import torch
+    import sparse_attention_td_gb300 as td
+    if not os.path.exists(td.lib_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wl = W.WORKLOADS[args.config]
+    if args.top_k:
+        wl = wl.with_(top_k=args.top_k)
+    layer = 2  # a selection layer of every 32-layer schedule
+    heavy = W.heavy_positions(wl)[layer]
+    lens = W.seq_lens(wl)
+    q, K, V = W.generate_layer(wl, layer, device, heavy)
+    seq = torch.as_tensor(lens).to(device)
+    shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len,
+                          scale=td.default_scale(wl.head_dim))
+    out = torch.empty_like(q)
+    idx = torch.full((wl.batch, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device=device)
+    ws = td.Workspace(shape, wl.top_k, device=device)
+    td.td_full_attn_select(shape, q, K, V, seq, wl.top_k, idx, out, None, None, ws)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def op():
+        if args.profile == "full":
+            td.td_full_attn_select(shape, q, K, V, seq, 0, None, out, None, None, ws)
+        elif args.profile == "select":
+            td.td_full_attn_select(shape, q, K, V, seq, wl.top_k, idx, out, None, None, ws)
+        else:
+            td.td_sparse_attn(shape, q, K, V, seq, idx, wl.top_k, out, None, ws)
+
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        op()
+        b.record()
+        if i >= args.warmup:
+            times.append((a, b))
+    torch.cuda.synchronize()
+    us = statistics.fmean(a.elapsed_time(b) for a, b in times) * 1e3
+    bm = step_bytes(wl, lens, [W.FULL])
+    nbytes = bm["per_launch"]["sparse" if args.profile == "sparse" else "full"]
+    assert ws.status() == 0
+    return {"profile": args.profile, "workload": wl.name, "top_k": wl.top_k, "launch_us": round(us, 2),
+            "algorithmic_bytes": nbytes, "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "splits": td.td_query_splits(shape, wl.top_k, args.profile == "sparse")}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,11 +525,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-groups", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", choices=["full", "select", "sparse"], default=None,
+                    help="time one layer's launch alone (small case for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
-    if args.impl == "reference":
+    if args.profile:
+        res = run_profile_layer(args, local)
+    elif args.impl == "reference":
         res = run_reference(args, world, rank, local)
     else:
         res = run_ours(args, world, rank, local)

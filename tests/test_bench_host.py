@@ -1,0 +1,66 @@
+"""Host logic of bench.py: byte model, clock parsing, and the max-over-ranks
+reduction on two gloo ranks (CPU, no GPU)."""
+import os
+import socket
+
+import numpy as np
+import torch.multiprocessing as mp
+
+import bench
+import workloads as W
+
+
+def test_step_bytes_model():
+    wl = W.WORKLOADS["llama2-7b-10k"]
+    lens = W.seq_lens(wl)
+    bm = bench.step_bytes(wl, lens, wl.modes)
+    assert bm["kv"]["full"] == 160 * 2**20                 # 32 heads x 10240 x 512 B
+    assert bm["kv"]["sparse"] == 8 * 2**20                 # 32 heads x 512 x 512 B
+    assert bm["step_kv"] == 4 * 160 * 2**20 + 28 * 8 * 2**20
+    tiny = W.WORKLOADS["tiny"]
+    bt = bench.step_bytes(tiny, W.seq_lens(tiny), tiny.modes)
+    assert bt["step_kv"] == 2 * 4 * 2**20 + 2 * 256 * 1024
+    # ragged lengths shorter than k count only their own tokens
+    short = tiny.with_(top_k=4096, max_seq_len=4096)
+    assert bench.step_bytes(short, np.array([100]), [W.SPARSE])["kv"]["sparse"] == 100 * 2 * 512
+
+
+def test_clock_summary_parses_nvidia_smi_rows():
+    c = bench.ClockSampler(0)
+    c.lines = ["0, 1965, 2070, 800.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 1980, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active",
+               "garbage"]
+    s = c.summary()
+    assert s["sm_mhz"] == 1972.5 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    bench.dist_init(world, "gloo")
+    got = bench.dist_max(10.0 + rank * 5.5, world)
+    bench.dist_barrier(world)
+    q.put((rank, got))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_dist_max_over_two_gloo_ranks():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res == {0: 15.5, 1: 15.5}
+
+
+def test_single_rank_is_identity():
+    assert bench.dist_max(3.25, 1) == 3.25
