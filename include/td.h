@@ -144,6 +144,37 @@ td_status td_sparse_attn(const td_shape *shape, const void *q, const void *k_cac
                          void *stream);
 
 /*
+ * td_sparse_attn for callers that cannot allocate device memory.  The paper
+ * has no counterpart: this is a deployment variant of the PPSA layer above,
+ * with the same arguments minus the workspace and the same result.
+ *
+ * Who needs it: code that may not call cudaMalloc or own a workspace -- a
+ * component inside a host framework that hands out all device memory from
+ * its own arena, a latency-critical path that must never enter the driver's
+ * allocator (it can synchronise the device), a plugin whose memory budget is
+ * fixed before it is loaded.  The entry point allocates nothing: its scratch
+ * (split partials, arrival tickets, status word) is one fixed array of
+ * TD_NOALLOC_SCRATCH_BYTES bytes inside the library's device image, which
+ * every GPU that loads the library keeps until the process exits.
+ *   - The first call on a device looks up the array's address (per device,
+ *     with that device current); make that first call before any stream
+ *     capture starts.
+ *   - Every call shares the array, which keeps the last call's contents; each
+ *     call clears the parts that must start at zero on its own stream.  Calls
+ *     whose kernels overlap on the GPU race on the array: keep them ordered on
+ *     one stream.
+ *   - Shapes whose scratch would exceed the array return
+ *     TD_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *   - Out-of-range index entries are skipped as in td_sparse_attn; this entry
+ *     point does not report the status word.
+ */
+#define TD_NOALLOC_SCRATCH_BYTES (8u << 20)
+td_status td_sparse_attn_noalloc(const td_shape *shape, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *seq_lens,
+                                 const int32_t *idx, int32_t top_k, void *out, float *out_f32,
+                                 void *stream);
+
+/*
  * One decode step over an L-layer attention-only stack (review §三 Figure 2).
  *   modes       HOST array [num_layers] of td_layer_mode.
  *   q, k_caches, v_caches, outs   HOST arrays of num_layers device pointers

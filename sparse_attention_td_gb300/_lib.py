@@ -76,6 +76,8 @@ def lib():
     L.td_topk_select.argtypes = [shp, vp, vp, i32, vp, vp, sz, vp]
     L.td_sparse_attn.restype = ctypes.c_int
     L.td_sparse_attn.argtypes = [shp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    L.td_sparse_attn_noalloc.restype = ctypes.c_int
+    L.td_sparse_attn_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
     L.td_decode_step.restype = ctypes.c_int
     L.td_decode_step.argtypes = [shp, i32, vp, vpp, vpp, vpp, vp, i32, vp, i32, vpp, vpp, vp, sz,
                                  vp, vpp]
@@ -215,6 +217,21 @@ def td_sparse_attn(shape: Shape, q, k_cache, v_cache, seq_lens, idx, top_k, out,
         _dev(out, "out", torch.bfloat16, nq), _dev(out_f32, "out_f32", torch.float32, nq, True),
         ws.ptr, ws.nbytes, _stream(stream))
     _check(st, "td_sparse_attn")
+
+
+def td_sparse_attn_noalloc(shape: Shape, q, k_cache, v_cache, seq_lens, idx, top_k, out,
+                           out_f32=None, stream=None):
+    """td_sparse_attn without a workspace, for callers that cannot allocate
+    device memory (scratch lives in a fixed array in the library)."""
+    nq, nkv, nb = _sizes(shape)
+    st = lib().td_sparse_attn_noalloc(
+        ctypes.byref(shape), _dev(q, "q", torch.bfloat16, nq),
+        _dev(k_cache, "k_cache", torch.bfloat16, nkv), _dev(v_cache, "v_cache", torch.bfloat16, nkv),
+        _dev(seq_lens, "seq_lens", torch.int32, nb),
+        _dev(idx, "idx", torch.int32, nb * shape.num_kv_heads * top_k), int(top_k),
+        _dev(out, "out", torch.bfloat16, nq), _dev(out_f32, "out_f32", torch.float32, nq, True),
+        _stream(stream))
+    _check(st, "td_sparse_attn_noalloc")
 
 
 def _ptr_array(tensors, name, dtype, numel, optional=False):
