@@ -18,6 +18,7 @@ constexpr int kMaxSplitCtas = 8192;    // cap on batch * kv_heads * splits for p
 constexpr int kMaxSparseChunk = 2048;  // index entries one sparse CTA stages in shared memory
 constexpr int kMaxTopK = kMaxSplits * kMaxSparseChunk;
 constexpr int kTopkThreads = 1024;
+constexpr int kTopkCandidates = 16384;  // (key, position) pairs a top-k CTA holds in shared memory
 
 constexpr uint32_t kFlagIndexOutOfRange = 0x1u;
 constexpr uint32_t kFlagSeqLenOutOfRange = 0x2u;

@@ -8,13 +8,20 @@
 // Ties at the k-th score go to the lower position; the result is written in
 // ascending position order and padded with -1 when seq_lens[b] < k.
 //
-// Method: exact radix select on order-preserving 32-bit keys.  Four passes
-// of 8-bit digits (most significant first) build a shared-memory histogram
-// of the keys that share the prefix found so far and pick the digit holding
-// the k-th largest key.  The result is the k-th key T and the number e of
-// keys equal to T that belong in the set.  A final pass, in position order,
-// keeps every key > T and the first e keys == T, with block-wide ballot
-// scans giving each kept position its output slot.
+// Method: exact radix select on order-preserving 32-bit keys, one 1024-thread
+// CTA per row, three reads of the row:
+//   1. an 11-bit histogram of the keys' top bits picks the bin holding the
+//      k-th largest key;
+//   2. that bin's (key, position) pairs are gathered into shared memory and
+//      the select finishes there: the k-th key T, and -- when only some of
+//      the keys equal to T fit in the set -- the largest position P that
+//      still does (the lowest positions win ties);
+//   3. an ordered compaction keeps every key > T and every key == T at a
+//      position <= P, with ballot-based block scans assigning output slots
+//      in position order.
+// Loads are batched eight per thread so each thread keeps eight in flight.
+// If the threshold bin is larger than the shared-memory buffer (heavily tied
+// scores), the remaining digits are selected by streaming passes instead.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,7 +31,12 @@ namespace td {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kWarps = kTopkThreads / 32;
+constexpr int kT = kTopkThreads;        // 1024
+constexpr int kWarps = kT / 32;         // 32
+constexpr int kBatch = 8;               // loads in flight per thread
+constexpr int kBits1 = 11;              // first digit: key bits 31..21
+constexpr int kBins1 = 1 << kBits1;     // 2048
+constexpr int kSubHists = 4;            // pass-1 sub-histograms (less atomic contention)
 
 // Order-preserving key: larger float -> larger unsigned.  -0.0 is mapped to
 // +0.0 first so the two tie.
@@ -36,36 +48,131 @@ __device__ __forceinline__ uint32_t order_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix count of `flag` over the block (thread order), plus the
-// block total.  Uses `warp_tot` (kWarps ints) as scratch; contains
-// __syncthreads, so every thread must call it.
-__device__ __forceinline__ int block_exclusive_count(bool flag, int *warp_tot, int &total)
+struct TopkSmem {
+    unsigned hist[kSubHists * kBins1];  // 32 KB; pass-1 sub-histograms, later one 256-bin histogram
+    unsigned scan[kWarps];
+    unsigned tot[kBatch * kWarps];
+    unsigned pre[kBatch * kWarps];
+    unsigned res[2];                    // digit, remaining rank
+    unsigned cand_count;
+};
+
+// Block-wide search over a histogram of NB bins (digit = bin index): the
+// digit d with count(> d) < r <= count(>= d).  Writes d and r - count(> d)
+// to sm.res.  All threads must call it.
+template <int NB>
+__device__ void find_digit(TopkSmem &sm, const unsigned *hist, unsigned r)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned bal = __ballot_sync(kFull, flag);
-    const int in_warp = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0)
-        warp_tot[warp] = __popc(bal);
-    __syncthreads();
-    int before = 0, all = 0;
-    for (int w = 0; w < kWarps; ++w) {
-        const int t = warp_tot[w];
-        before += (w < warp) ? t : 0;
-        all += t;
+    constexpr int per = NB >= kT ? NB / kT : 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int first = NB - 1 - tid * per;  // this thread's highest bin
+    unsigned c = 0;
+    if (first >= 0)
+        for (int i = 0; i < per; ++i)
+            c += hist[first - i];
+    unsigned incl = c;
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned v = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off)
+            incl += v;
     }
-    __syncthreads();  // warp_tot is reused by the next call
-    total = all;
-    return before + in_warp;
+    if (lane == 31)
+        sm.scan[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned w = sm.scan[lane], wi = w;
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned v = __shfl_up_sync(kFull, wi, off);
+            if (lane >= off)
+                wi += v;
+        }
+        sm.scan[lane] = wi - w;  // exclusive offset of each warp
+    }
+    __syncthreads();
+    incl += sm.scan[warp];
+    const unsigned excl = incl - c;
+    if (c > 0 && excl < r && r <= incl) {
+        unsigned run = excl;
+        for (int i = 0; i < per; ++i) {
+            const unsigned h = hist[first - i];
+            if (run + h >= r) {
+                sm.res[0] = (unsigned)(first - i);
+                sm.res[1] = r - run;
+                break;
+            }
+            run += h;
+        }
+    }
+    __syncthreads();
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
+// Calls f(key, pos) for every position of the row, eight loads in flight per thread.
+template <class F>
+__device__ __forceinline__ void stream_row(const float *s, int n, F f)
+{
+    for (int base = 0; base < n; base += kT * kBatch) {
+        float v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = base + j * kT + (int)threadIdx.x;
+            v[j] = i < n ? __ldcg(&s[i]) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = base + j * kT + (int)threadIdx.x;
+            if (i < n)
+                f(order_key(v[j]), i);
+        }
+    }
+}
+
+// Radix select over a stream of (value, item) pairs that pass `keep`: the
+// r-th largest value among them, digits of 8 bits over bits [hi_bit..0],
+// starting from `prefix`/`mask` (bits already fixed).  `src(f)` must call f
+// for every pair.  Returns the value; *rank_out receives r minus the count of
+// larger values (how many items equal to the result belong in the set) and
+// *eq_out the number of items equal to it.
+template <class Src>
+__device__ uint32_t radix_select(TopkSmem &sm, Src src, int hi_bit, uint32_t prefix,
+                                 uint32_t mask, unsigned r, unsigned *rank_out, unsigned *eq_out)
+{
+    unsigned *hist = sm.hist;
+    unsigned last_count = 0;
+    for (int top = hi_bit; top >= 0; top -= 8) {
+        const int width = top + 1 < 8 ? top + 1 : 8;
+        const int shift = top + 1 - width;
+        const unsigned dmask = (1u << width) - 1u;
+        for (int i = threadIdx.x; i < 256; i += kT)
+            hist[i] = 0u;
+        __syncthreads();
+        src([&](uint32_t val, int) {
+            if ((val & mask) == prefix)
+                atomicAdd(&hist[(val >> shift) & dmask], 1u);
+        });
+        __syncthreads();
+        find_digit<256>(sm, hist, r);
+        const unsigned d = sm.res[0];
+        r = sm.res[1];
+        last_count = hist[d];
+        prefix |= d << shift;
+        mask |= dmask << shift;
+        __syncthreads();
+    }
+    *rank_out = r;
+    *eq_out = last_count;
+    return prefix;
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 1)
 topk_kernel(const TopkArgs a)
 {
-    __shared__ unsigned hist[256];
-    __shared__ unsigned sh_digit, sh_krem;
-    __shared__ int warp_tot[kWarps];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    TopkSmem &sm = *reinterpret_cast<TopkSmem *>(smem_raw);
+    uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem_raw + sizeof(TopkSmem));
+    int32_t *cand_pos = reinterpret_cast<int32_t *>(cand_key + kTopkCandidates);
 
     const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     const size_t bg = (size_t)b * a.Hkv + g;
     const int k = a.top_k;
     int n = a.seq_lens[b];
@@ -78,84 +185,185 @@ topk_kernel(const TopkArgs a)
     int32_t *out = a.idx + bg * (size_t)k;
 
     if (n <= k) {  // every position is kept
-        for (int j = tid; j < k; j += kTopkThreads)
+        for (int j = tid; j < k; j += kT)
             out[j] = j < n ? j : -1;
         return;
     }
 
-    uint32_t prefix = 0u, mask = 0u;
-    unsigned krem = (unsigned)k;  // how many of the keys matching `prefix` still belong in the set
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += kTopkThreads)
-            hist[i] = 0u;
-        __syncthreads();
-        for (int i = tid; i < n; i += kTopkThreads) {
-            const uint32_t key = order_key(__ldcg(&s[i]));
-            if ((key & mask) == prefix)
-                atomicAdd(&hist[(key >> shift) & 255u], 1u);
-        }
-        __syncthreads();
-        if (tid < 32) {
-            // lane j owns bins 255-8j down to 248-8j; scan from the top bin down
-            const int lane = tid;
-            unsigned mine = 0u;
-            for (int i = 0; i < 8; ++i)
-                mine += hist[255 - 8 * lane - i];
-            unsigned incl = mine;
-            for (int off = 1; off < 32; off <<= 1) {
-                const unsigned v = __shfl_up_sync(kFull, incl, off);
-                if (lane >= off)
-                    incl += v;
+    // 1. histogram of the top 11 bits
+    for (int i = tid; i < kSubHists * kBins1; i += kT)
+        sm.hist[i] = 0u;
+    if (tid == 0)
+        sm.cand_count = 0u;
+    __syncthreads();
+    {
+        unsigned *mine = sm.hist + (warp % kSubHists) * kBins1;
+        stream_row(s, n, [&](uint32_t key, int) { atomicAdd(&mine[key >> (32 - kBits1)], 1u); });
+    }
+    __syncthreads();
+    for (int i = tid; i < kBins1; i += kT) {
+        unsigned t = 0;
+        for (int h = 0; h < kSubHists; ++h)
+            t += sm.hist[h * kBins1 + i];
+        sm.hist[i] = t;
+    }
+    __syncthreads();
+    find_digit<kBins1>(sm, sm.hist, (unsigned)k);
+    const uint32_t d1 = sm.res[0];
+    const unsigned r1 = sm.res[1];
+    const unsigned bin_count = sm.hist[d1];
+    __syncthreads();
+
+    const uint32_t prefix1 = d1 << (32 - kBits1);
+    const uint32_t mask1 = ~0u << (32 - kBits1);
+    uint32_t T;
+    unsigned need_eq, n_eq;
+    int P = 0x7fffffff;  // largest kept position among keys == T
+    if (bin_count <= (unsigned)kTopkCandidates) {
+        // 2. gather the threshold bin into shared memory, finish there
+        for (int base = 0; base < n; base += kT * kBatch) {
+            float v[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int i = base + j * kT + tid;
+                v[j] = i < n ? __ldcg(&s[i]) : 0.0f;
             }
-            const unsigned excl = incl - mine;
-            if (excl < krem && krem <= incl) {
-                unsigned run = excl;
-                for (int i = 0; i < 8; ++i) {
-                    const int bin = 255 - 8 * lane - i;
-                    if (run + hist[bin] >= krem) {
-                        sh_digit = (unsigned)bin;
-                        sh_krem = krem - run;
-                        break;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int i = base + j * kT + tid;
+                const uint32_t key = order_key(v[j]);
+                const bool hit = i < n && (key & mask1) == prefix1;
+                const unsigned m = __ballot_sync(kFull, hit);
+                if (m) {  // warp-uniform
+                    unsigned slot0 = 0;
+                    if (lane == 0)
+                        slot0 = atomicAdd(&sm.cand_count, (unsigned)__popc(m));
+                    slot0 = __shfl_sync(kFull, slot0, 0);
+                    if (hit) {
+                        const unsigned slot = slot0 + __popc(m & ((1u << lane) - 1u));
+                        cand_key[slot] = key;
+                        cand_pos[slot] = i;
                     }
-                    run += hist[bin];
                 }
             }
         }
         __syncthreads();
-        prefix |= sh_digit << shift;
-        mask |= 255u << shift;
-        krem = sh_krem;
-        __syncthreads();
+        const unsigned cnt = sm.cand_count;
+        auto cand_src = [&](auto f) {
+            for (unsigned i = tid; i < cnt; i += kT)
+                f(cand_key[i], cand_pos[i]);
+        };
+        T = radix_select(sm, cand_src, 31 - kBits1, prefix1, mask1, r1, &need_eq, &n_eq);
+        if (need_eq < n_eq) {
+            // lowest positions win: the need_eq-th largest of ~pos among keys == T
+            auto eq_src = [&](auto f) {
+                for (unsigned i = tid; i < cnt; i += kT)
+                    if (cand_key[i] == T)
+                        f(~(uint32_t)cand_pos[i], 0);
+            };
+            unsigned r_dummy, e_dummy;
+            P = (int)~radix_select(sm, eq_src, 31, 0u, 0u, need_eq, &r_dummy, &e_dummy);
+        }
+    } else {
+        // threshold bin too large for shared memory: stream the remaining digits
+        auto row_src = [&](auto f) { stream_row(s, n, f); };
+        T = radix_select(sm, row_src, 31 - kBits1, prefix1, mask1, r1, &need_eq, &n_eq);
+        if (need_eq < n_eq) {
+            auto eq_src = [&](auto f) {
+                stream_row(s, n, [&](uint32_t key, int i) {
+                    if (key == T)
+                        f(~(uint32_t)i, 0);
+                });
+            };
+            unsigned r_dummy, e_dummy;
+            P = (int)~radix_select(sm, eq_src, 31, 0u, 0u, need_eq, &r_dummy, &e_dummy);
+        }
     }
-    // prefix is now the k-th largest key T; krem keys equal to T are kept.
-    const uint32_t T = prefix;
-    const int need_eq = (int)krem;
-    int out_base = 0, eq_base = 0;
-    for (int tile = 0; tile < n; tile += kTopkThreads) {
-        const int i = tile + tid;
-        uint32_t key = 0u;
-        if (i < n)
-            key = order_key(__ldcg(&s[i]));
-        const bool gt = i < n && key > T;
-        const bool eq = i < n && key == T;
-        int eq_total = 0, take_total = 0;
-        const int eq_rank = eq_base + block_exclusive_count(eq, warp_tot, eq_total);
-        const bool take = gt || (eq && eq_rank < need_eq);
-        const int slot = out_base + block_exclusive_count(take, warp_tot, take_total);
-        if (take && slot < k)  // exactly k are taken; the bound only guards memory
-            out[slot] = i;
-        out_base += take_total;
-        eq_base += eq_total;
+    __syncthreads();
+
+    // 3. ordered compaction: keys > T, and keys == T at positions <= P
+    unsigned out_base = 0;
+    for (int base = 0; base < n; base += kT * kBatch) {
+        float v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = base + j * kT + tid;
+            v[j] = i < n ? __ldcg(&s[i]) : 0.0f;
+        }
+        unsigned bal[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = base + j * kT + tid;
+            const uint32_t key = order_key(v[j]);
+            const bool take = i < n && (key > T || (key == T && i <= P));
+            bal[j] = __ballot_sync(kFull, take);
+            if (lane == 0)
+                sm.tot[j * kWarps + warp] = __popc(bal[j]);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // exclusive scan of the 256 counts in (j, warp) order = position order
+            unsigned c[8], sum = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                c[e] = sm.tot[lane * 8 + e];
+                sum += c[e];
+            }
+            unsigned incl = sum;
+            for (int off = 1; off < 32; off <<= 1) {
+                const unsigned t = __shfl_up_sync(kFull, incl, off);
+                if (lane >= off)
+                    incl += t;
+            }
+            unsigned run = incl - sum;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                sm.pre[lane * 8 + e] = run;
+                run += c[e];
+            }
+            if (lane == 31)
+                sm.res[0] = incl;  // super-tile total
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (bal[j] & (1u << lane)) {
+                const unsigned slot = out_base + sm.pre[j * kWarps + warp] +
+                                      __popc(bal[j] & ((1u << lane) - 1u));
+                if (slot < (unsigned)k)  // exactly k are taken; the bound only guards memory
+                    out[slot] = base + j * kT + tid;
+            }
+        }
+        out_base += sm.res[0];
+        __syncthreads();
     }
 }
 
 }  // namespace
 
+size_t topk_smem_bytes()
+{
+    return sizeof(TopkSmem) + (size_t)kTopkCandidates * (sizeof(uint32_t) + sizeof(int32_t));
+}
+
 cudaError_t launch_topk(const TopkArgs &a, int batch, cudaStream_t stream)
 {
+    const size_t smem = topk_smem_bytes();
+    static bool configured[64] = {false};  // the smem opt-in is per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < 64)
+            configured[dev] = true;
+    }
     dim3 grid((unsigned)a.Hkv, (unsigned)batch);
-    topk_kernel<<<grid, kTopkThreads, 0, stream>>>(a);
+    topk_kernel<<<grid, kTopkThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -160,6 +160,22 @@ def test_topk_large_rows(orc):
         assert np.array_equal(got[b, 0], want), f"row {b}"
 
 
+def test_topk_threshold_bin_larger_than_shared_memory(orc):
+    """More than 16384 scores share the threshold's top bits: the kernel's
+    streaming fallback path (heavy ties at and around the k-th score)."""
+    rs = np.random.RandomState(7)
+    N = 60000
+    rows = [np.zeros(N, np.float32),                                   # one bin, all tied
+            rs.randint(0, 2, N).astype(np.float32),                    # two values
+            (1.0 + rs.randint(0, 64, N) * 2.0 ** -20).astype(np.float32)]  # one 11-bit bin, 64 values
+    lens = [N, N - 3, N]
+    for k in (1, 1000, 30001):
+        arr, got = _topk_case(rows, lens, k)
+        for b in range(len(rows)):
+            want = orc.topk(arr[b, 0, :lens[b]].astype(np.float64), k)
+            assert np.array_equal(got[b, 0], want), f"row {b} k={k}"
+
+
 def run_sparse(shape, q, K, V, lens, idx_np, top_k):
     qd, Kd, Vd = _dev(q, K, V)
     seq = torch.as_tensor(np.asarray(lens, np.int32)).cuda()
