@@ -25,7 +25,7 @@ using td::kHeadDim;
 struct Tuning {
     int full_ctas_per_sm = 0;    // 0 = occupancy query
     int sparse_ctas_per_sm = 0;
-    int full_waves = 2;
+    int full_waves = 0;          // 0 = auto (see plan_splits)
     int sparse_waves = 1;
     int max_splits = td::kMaxSplits;
 };
@@ -161,19 +161,22 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
     int per_sm = sparse ? g_tuning.sparse_ctas_per_sm : g_tuning.full_ctas_per_sm;
     if (per_sm <= 0)
         per_sm = td::attention_ctas_per_sm(G, sparse, select);
-    const int waves = sparse ? g_tuning.sparse_waves : g_tuning.full_waves;
-    const long target = (long)device_sm_count() * per_sm * (waves > 0 ? waves : 1);
+    const long slots = (long)device_sm_count() * per_sm;  // resident CTAs per wave
+    int waves = sparse ? g_tuning.sparse_waves : g_tuning.full_waves;
+    if (waves <= 0)  // one wave of long CTAs when the pairs are few; more, shorter
+        waves = units * 2 <= slots ? 1 : 3;  // CTAs balance ragged lengths otherwise
+    const long target = slots * waves;
     const int cap = split_cap(units, n_total, sparse);
-    long want = ceil_div(target, units);
+    long want = target / units;  // whole waves: never spill a few CTAs into an extra wave
     if (want < 1) want = 1;
     if (want > cap) want = cap;
     const long len = n_total > 0 ? n_total : 1;
-    long ch = ceil_div(ceil_div(len, want), td::kTokPerRound) * td::kTokPerRound;
+    long ch = ceil_div(ceil_div(len, want), td::kChunkGranule) * td::kChunkGranule;
     if (sparse && ch > td::kMaxSparseChunk)
         ch = td::kMaxSparseChunk;
     long ns = ceil_div(len, ch);
     if (ns > cap) {  // rounding pushed past the cap: widen the chunk instead
-        ch = ceil_div(ceil_div(len, cap), td::kTokPerRound) * td::kTokPerRound;
+        ch = ceil_div(ceil_div(len, cap), td::kChunkGranule) * td::kChunkGranule;
         ns = ceil_div(len, ch);
     }
     nsplit = (int)ns;

@@ -53,6 +53,20 @@ __device__ __forceinline__ uint4 load_row16(const uint16_t *p)
     return r;
 }
 
+// Programmatic dependent launch: a kernel of the next layer may start while
+// this one finishes.  Before pdl_wait() a kernel touches only inputs no kernel
+// of the step writes (seq_lens, q, the K/V cache); after it, everything the
+// previous kernel wrote (index set, scores, workspace) is complete and visible.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float safe_exp2_diff(float x, float m)
 {
     // exp2(x - m) with m = -inf meaning "no token seen yet" (weight 0)
@@ -103,6 +117,8 @@ attention_kernel(const AttnArgs a)
     const uint16_t *vbase = a.v + bg * (size_t)a.Nmax * kHeadDim + c * 8;
 
     if constexpr (SPARSE) {
+        // The index set may come from the kernel just before this one.
+        pdl_wait();
         // Stage this split's persisted positions; -1 is padding, anything
         // else outside [0, n_b) is reported and skipped.
         const int32_t *ip = a.idx + bg * (size_t)a.top_k;
@@ -156,6 +172,8 @@ attention_kernel(const AttnArgs a)
                 vr[u] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
+        if (!SPARSE && base == t0)
+            pdl_wait();  // first K/V rows are in flight; from here on scores may be written
 
         // q . k over this lane's 8 dims, then over the half-warp's 16 lanes.
         float dot[G][U];
@@ -239,6 +257,9 @@ attention_kernel(const AttnArgs a)
                     o[h][i] = fmaf(p[h][u], vf[i], o[h][i]);
         }
     }
+
+    pdl_wait();              // (no-op if already waited; covers empty ranges)
+    pdl_launch_dependents(); // the next layer's CTAs may start loading its cache
 
     // Merge the two half-warps, then the 8 warps, of this CTA.
 #pragma unroll
@@ -402,9 +423,17 @@ attention_kernel(const AttnArgs a)
 template <int G, bool SPARSE, bool SELECT>
 cudaError_t launch_one(const AttnArgs &a, int batch, cudaStream_t stream)
 {
-    dim3 grid((unsigned)a.nsplit, (unsigned)a.Hkv, (unsigned)batch);
-    attention_kernel<G, SPARSE, SELECT><<<grid, kAttnThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.nsplit, (unsigned)a.Hkv, (unsigned)batch);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attention_kernel<G, SPARSE, SELECT>, a);
 }
 
 template <int G, bool SPARSE, bool SELECT>

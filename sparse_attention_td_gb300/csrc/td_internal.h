@@ -11,8 +11,9 @@ namespace td {
 constexpr int kHeadDim = 128;          // only head_dim supported
 constexpr int kAttnThreads = 256;      // 8 warps
 constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kTokPerHalf = 4;         // tokens a half-warp holds in flight per round
+constexpr int kTokPerHalf = 4;         // tokens a half-warp handles per round
 constexpr int kTokPerRound = kAttnWarps * 2 * kTokPerHalf;  // 64 tokens per CTA round
+constexpr int kChunkGranule = 16;      // split lengths are multiples of this many tokens
 constexpr int kMaxSplits = 256;        // splits per (batch, KV head)
 constexpr int kMaxSplitCtas = 8192;    // cap on batch * kv_heads * splits for partials
 constexpr int kMaxSparseChunk = 2048;  // index entries one sparse CTA stages in shared memory

@@ -38,6 +38,19 @@ constexpr int kBits1 = 11;              // first digit: key bits 31..21
 constexpr int kBins1 = 1 << kBits1;     // 2048
 constexpr int kSubHists = 4;            // pass-1 sub-histograms (less atomic contention)
 
+// Programmatic dependent launch (see td_attn.cu): the scores come from the
+// kernel just before this one, so wait for it; the next layer's kernel may
+// launch right away (it waits for this one before reading the index set).
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Order-preserving key: larger float -> larger unsigned.  -0.0 is mapped to
 // +0.0 first so the two tie.
 __device__ __forceinline__ uint32_t order_key(float f)
@@ -183,6 +196,8 @@ topk_kernel(const TopkArgs a)
     }
     const float *s = a.scores + bg * (size_t)a.Nmax;
     int32_t *out = a.idx + bg * (size_t)k;
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (n <= k) {  // every position is kept
         for (int j = tid; j < k; j += kT)
@@ -362,9 +377,17 @@ cudaError_t launch_topk(const TopkArgs &a, int batch, cudaStream_t stream)
         if (dev >= 0 && dev < 64)
             configured[dev] = true;
     }
-    dim3 grid((unsigned)a.Hkv, (unsigned)batch);
-    topk_kernel<<<grid, kTopkThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)batch);
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_kernel, a);
 }
 
 }  // namespace td
