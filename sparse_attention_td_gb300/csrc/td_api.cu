@@ -272,13 +272,16 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
     return TD_OK;
 }
 
+// idx_dep: the kernel launched just before may have written `idx` (then the
+// sparse kernel waits for it before reading the set).
 td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
                      const int32_t *seq_lens, const int32_t *idx, int top_k, void *out,
-                     float *out_f32, cudaStream_t st)
+                     float *out_f32, cudaStream_t st, bool idx_dep)
 {
     td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
     a.idx = idx;
     a.top_k = top_k;
+    a.idx_dep = idx_dep ? 1 : 0;
     plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
     if (td::launch_attention(c.G, true, false, a, c.shape.batch, st) != cudaSuccess)
         return TD_ERR_CUDA;
@@ -347,7 +350,7 @@ td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
             break;
         default:
             r = run_sparse(c, q[l], k_caches[l], v_caches[l], seq_lens, idx_buf, top_k, outs[l],
-                           of, st);
+                           of, st, l == 0 || modes[l - 1] == TD_MODE_FULL_SELECT);
             break;
         }
         if (r)
@@ -473,7 +476,7 @@ td_status td_sparse_attn(const td_shape *shape, const void *q, const void *k_cac
     if (top_k < 1 || !idx || !aligned(idx, 4) || !seq_lens || !aligned(seq_lens, 4))
         return TD_ERR_INVALID_ARG;
     return run_sparse(c, q, k_cache, v_cache, seq_lens, idx, top_k, out, out_f32,
-                      (cudaStream_t)stream);
+                      (cudaStream_t)stream, true);
 }
 
 td_status td_decode_step(const td_shape *shape, int32_t num_layers, const int32_t *modes,

@@ -53,10 +53,12 @@ __device__ __forceinline__ uint4 load_row16(const uint16_t *p)
     return r;
 }
 
-// Programmatic dependent launch: a kernel of the next layer may start while
-// this one finishes.  Before pdl_wait() a kernel touches only inputs no kernel
-// of the step writes (seq_lens, q, the K/V cache); after it, everything the
-// previous kernel wrote (index set, scores, workspace) is complete and visible.
+// Programmatic dependent launch: the next kernel of the step may start while
+// this one finishes.  Before pdl_wait() a kernel touches only what no kernel
+// of the step writes (seq_lens, the K/V cache, and an index set produced
+// earlier than by the kernel right before); after it, everything the
+// previous kernel wrote (q in a full model, index set, scores, workspace) is
+// complete and visible.
 __device__ __forceinline__ void pdl_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -117,8 +119,10 @@ attention_kernel(const AttnArgs a)
     const uint16_t *vbase = a.v + bg * (size_t)a.Nmax * kHeadDim + c * 8;
 
     if constexpr (SPARSE) {
-        // The index set may come from the kernel just before this one.
-        pdl_wait();
+        // The index set was computed earlier in the step, unless the kernel
+        // right before this one produced it: then wait for that kernel first.
+        if (a.idx_dep)
+            pdl_wait();
         // Stage this split's persisted positions; -1 is padding, anything
         // else outside [0, n_b) is reported and skipped.
         const int32_t *ip = a.idx + bg * (size_t)a.top_k;
@@ -132,6 +136,28 @@ attention_kernel(const AttnArgs a)
         }
         __syncthreads();
     }
+
+    // This half-warp's U tokens of the round starting at `base`: K and V rows
+    // requested into registers (zero for tokens past the split or padding).
+    auto load_round = [&](int base, uint4 (&kr)[U], uint4 (&vr)[U], bool (&ok)[U]) {
+        const int tb = base + (warp * 2 + half) * U;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = tb + u;
+            int row = -1;
+            if (t < t1)
+                row = SPARSE ? sm_rows[t - t0] : t;
+            ok[u] = row >= 0;
+            kr[u] = ok[u] ? load_row16(kbase + (size_t)row * kHeadDim) : make_uint4(0u, 0u, 0u, 0u);
+            vr[u] = ok[u] ? load_row16(vbase + (size_t)row * kHeadDim) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    // The cache is never written by a kernel of the step, so the first round
+    // is requested before waiting for the previous kernel; q may come from it.
+    uint4 kr0[U], vr0[U];
+    bool ok0[U];
+    load_round(t0, kr0, vr0, ok0);
+    pdl_wait();
 
     // This lane's 8 dims of the group's G queries.
     float qf[G][8];
@@ -153,27 +179,9 @@ attention_kernel(const AttnArgs a)
             o[h][i] = 0.0f;
     }
 
-    for (int base = t0; base < t1; base += kTokPerRound) {
+    // One round: scores, online softmax and P V for this half-warp's U tokens.
+    auto round = [&](int base, const uint4 (&kr)[U], const uint4 (&vr)[U], const bool (&ok)[U]) {
         const int tb = base + (warp * 2 + half) * U;  // this half-warp's first token
-        uint4 kr[U], vr[U];
-        bool ok[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int t = tb + u;
-            int row = -1;
-            if (t < t1)
-                row = SPARSE ? sm_rows[t - t0] : t;
-            ok[u] = row >= 0;
-            if (ok[u]) {
-                kr[u] = load_row16(kbase + (size_t)row * kHeadDim);
-                vr[u] = load_row16(vbase + (size_t)row * kHeadDim);
-            } else {
-                kr[u] = make_uint4(0u, 0u, 0u, 0u);
-                vr[u] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        if (!SPARSE && base == t0)
-            pdl_wait();  // first K/V rows are in flight; from here on scores may be written
 
         // q . k over this lane's 8 dims, then over the half-warp's 16 lanes.
         float dot[G][U];
@@ -256,10 +264,17 @@ attention_kernel(const AttnArgs a)
                 for (int i = 0; i < 8; ++i)
                     o[h][i] = fmaf(p[h][u], vf[i], o[h][i]);
         }
+    };
+    if (t0 < t1)
+        round(t0, kr0, vr0, ok0);
+    for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
+        uint4 kr[U], vr[U];
+        bool ok[U];
+        load_round(base, kr, vr, ok);
+        round(base, kr, vr, ok);
     }
 
-    pdl_wait();              // (no-op if already waited; covers empty ranges)
-    pdl_launch_dependents(); // the next layer's CTAs may start loading its cache
+    pdl_launch_dependents();  // the next kernel's CTAs may start requesting their cache rows
 
     // Merge the two half-warps, then the 8 warps, of this CTA.
 #pragma unroll

@@ -41,6 +41,7 @@ struct AttnArgs {
     uint32_t *tickets;       // [B*Hkv] arrival counters, zero between launches
     uint32_t *status;        // device status word
     int Hq, Hkv, Nmax, top_k;
+    int idx_dep;             // sparse: the index set may be written by the previous kernel
     int chunk;               // tokens (full) or index entries (sparse) per split
     int nsplit;              // gridDim.x
     float scale;             // softmax scale (natural-log units)

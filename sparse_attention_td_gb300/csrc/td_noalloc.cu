@@ -155,6 +155,7 @@ extern "C" td_status td_sparse_attn_noalloc(const td_shape *shape, const void *q
     a.Hkv = s.num_kv_heads;
     a.Nmax = s.max_seq_len;
     a.top_k = top_k;
+    a.idx_dep = 1;
     a.chunk = chunk;
     a.nsplit = nsplit;
     a.scale = s.scale != 0.0f ? s.scale : 1.0f / sqrtf((float)s.head_dim);
