@@ -223,6 +223,10 @@ void td_plan_destroy(td_plan *plan);
  *   "full_ctas_per_sm", "sparse_ctas_per_sm": resident CTAs assumed per SM
  *   "full_waves", "sparse_waves": target waves of CTAs per launch
  *   "max_splits": upper bound on splits per (batch, KV head)
+ *   "cluster": 1 merges a (batch, KV head)'s splits (when 2..8) through a
+ *              thread-block cluster; 0 (default) through global partials
+ *   "attn_carveout": preferred shared-memory carveout of the attention kernels
+ *                    in percent (0..100; negative = driver default)
  * value <= 0 restores the default.  Unknown key -> TD_ERR_INVALID_ARG.
  */
 td_status td_set_tuning(const char *key, int32_t value);

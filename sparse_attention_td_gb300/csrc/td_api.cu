@@ -28,6 +28,7 @@ struct Tuning {
     int full_waves = 0;          // 0 = auto (see plan_splits)
     int sparse_waves = 1;
     int max_splits = td::kMaxSplits;
+    int cluster = 0;             // 1: merge up to kPortableClusterSplits splits through a cluster
 };
 Tuning g_tuning;
 const Tuning kDefaultTuning;
@@ -84,7 +85,7 @@ long partial_slots(const td_shape &s, int top_k)
 }
 
 struct WsLayout {
-    size_t status, tickets, part_m, part_l, part_o, scores, total;
+    size_t status, tickets, part_m, part_l, part_o, scores, hist, total;
 };
 
 WsLayout ws_layout(const td_shape &s, int top_k)
@@ -107,6 +108,9 @@ WsLayout ws_layout(const td_shape &s, int top_k)
     w.scores = off;
     if (top_k > 0)
         off = align_up(off + units * (size_t)s.max_seq_len * sizeof(float));
+    w.hist = off;  // first-digit histograms of a selection layer (kept zero between uses)
+    if (top_k > 0)
+        off = align_up(off + units * (size_t)td::kSelectBins * sizeof(unsigned));
     w.total = off;
     return w;
 }
@@ -254,12 +258,15 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
     const bool select = top_k > 0;
     td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
     a.scores = select ? (scores_out ? scores_out : (float *)(c.wsb + c.ws.scores)) : nullptr;
+    a.hist = select ? (unsigned *)(c.wsb + c.ws.hist) : nullptr;
     plan_splits(c.shape, c.shape.max_seq_len, false, select, a.nsplit, a.chunk);
-    if (td::launch_attention(c.G, false, select, a, c.shape.batch, st) != cudaSuccess)
+    const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
+    if (td::launch_attention(c.G, false, select, cluster, a, c.shape.batch, st) != cudaSuccess)
         return TD_ERR_CUDA;
     if (select) {
         td::TopkArgs t{};
         t.scores = a.scores;
+        t.hist = a.hist;
         t.seq_lens = seq_lens;
         t.idx = idx_out;
         t.status = a.status;
@@ -283,7 +290,8 @@ td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
     a.top_k = top_k;
     a.idx_dep = idx_dep ? 1 : 0;
     plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
-    if (td::launch_attention(c.G, true, false, a, c.shape.batch, st) != cudaSuccess)
+    const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
+    if (td::launch_attention(c.G, true, false, cluster, a, c.shape.batch, st) != cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }
@@ -583,6 +591,10 @@ td_status td_set_tuning(const char *key, int32_t value)
         g_tuning.full_waves = value > 0 ? value : kDefaultTuning.full_waves;
     else if (!strcmp(key, "sparse_waves"))
         g_tuning.sparse_waves = value > 0 ? value : kDefaultTuning.sparse_waves;
+    else if (!strcmp(key, "cluster"))
+        g_tuning.cluster = value > 0 ? 1 : 0;
+    else if (!strcmp(key, "attn_carveout"))
+        td::set_attention_carveout(value >= 0 && value <= 100 ? value : -1);
     else if (!strcmp(key, "max_splits"))
         g_tuning.max_splits = (value > 0 && value <= td::kMaxSplits) ? value : td::kMaxSplits;
     else

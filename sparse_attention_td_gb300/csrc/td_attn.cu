@@ -17,6 +17,7 @@
 // core path: each half-warp reads one 256-byte K row and one V row with
 // 16-byte loads (lane c holds dims 8c..8c+7), every thread keeps 4 tokens of
 // K and V in flight, and dot products are reduced with warp shuffles.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -69,6 +70,16 @@ __device__ __forceinline__ void pdl_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Order-preserving 32-bit key of a score (as in the top-k kernel): larger
+// float -> larger unsigned, -0.0 equal to +0.0.
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u)
+        u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 __device__ __forceinline__ float safe_exp2_diff(float x, float m)
 {
     // exp2(x - m) with m = -inf meaning "no token seen yet" (weight 0)
@@ -80,7 +91,12 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f)
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-template <int G, bool SPARSE, bool SELECT>
+namespace cg = cooperative_groups;
+
+// CLUSTER: the splits of one (batch row, KV head) form a thread-block
+// cluster (grid x = cluster x = splits) and are merged through distributed
+// shared memory; otherwise through global partials and an arrival ticket.
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER>
 __global__ void __launch_bounds__(kAttnThreads)
 attention_kernel(const AttnArgs a)
 {
@@ -94,6 +110,8 @@ attention_kernel(const AttnArgs a)
     __shared__ float sm_red[kAttnWarps][G];
     __shared__ int sm_rows[SPARSE ? kMaxSparseChunk : 1];
     __shared__ int sm_last;
+    // selection layers: histogram of the scores' top 11 bits (the top-k kernel's first digit)
+    __shared__ unsigned sm_hist[SELECT ? kSelectBins : 1];
     // per-split merge weights of the final combine; sm_o is dead by then
     static_assert(kMaxSplits <= kAttnWarps * kHeadDim, "sm_sw must fit in sm_o");
     float *sm_sw = &sm_o[0][0][0];
@@ -110,14 +128,22 @@ attention_kernel(const AttnArgs a)
     }
     const int n_total = SPARSE ? a.top_k : n_b;
     const int nsplit_b = n_total > 0 ? (n_total + a.chunk - 1) / a.chunk : 1;
-    if (split >= nsplit_b)
+    // A split past this row's work returns at once -- except in a cluster,
+    // where it takes part in the merge with an empty range.
+    const bool idle = split >= nsplit_b;
+    if (idle && !CLUSTER)
         return;
-    const int t0 = split * a.chunk;
-    const int t1 = min(t0 + a.chunk, n_total);
+    const int t0 = idle ? 0 : split * a.chunk;
+    const int t1 = idle ? 0 : min(t0 + a.chunk, n_total);
     const size_t bg = (size_t)b * a.Hkv + g;
     const uint16_t *kbase = a.k + bg * (size_t)a.Nmax * kHeadDim + c * 8;
     const uint16_t *vbase = a.v + bg * (size_t)a.Nmax * kHeadDim + c * 8;
 
+    if constexpr (SELECT) {
+        for (int i = tid; i < kSelectBins; i += kAttnThreads)
+            sm_hist[i] = 0u;
+        __syncthreads();
+    }
     if constexpr (SPARSE) {
         // The index set was computed earlier in the step, unless the kernel
         // right before this one produced it: then wait for that kernel first.
@@ -219,8 +245,10 @@ attention_kernel(const AttnArgs a)
                 if (c == u)
                     sc = s;
             }
-            if (c < U && tb + c < t1)
+            if (c < U && tb + c < t1) {
                 a.scores[bg * (size_t)a.Nmax + tb + c] = sc;
+                atomicAdd(&sm_hist[order_key(sc) >> (32 - kSelectBits)], 1u);
+            }
         }
 
         // Online softmax over this round's U tokens, then P V.
@@ -305,6 +333,12 @@ attention_kernel(const AttnArgs a)
         }
     }
     __syncthreads();
+    if constexpr (SELECT) {
+        unsigned *gh = a.hist + bg * kSelectBins;
+        for (int i = tid; i < kSelectBins; i += kAttnThreads)
+            if (sm_hist[i])
+                atomicAdd(&gh[i], sm_hist[i]);
+    }
     if (tid < G) {
         const int h = tid;
         float M = -CUDART_INF_F;
@@ -322,6 +356,62 @@ attention_kernel(const AttnArgs a)
     __syncthreads();
 
     const size_t out_row0 = (size_t)b * a.Hq + (size_t)g * G;  // first query head of the group
+    if constexpr (CLUSTER) {
+        // This split's partial (un-normalised o, M, L) stays in shared
+        // memory: o in sm_o[0], M and L in sm_M / sm_L.
+        constexpr int PER = (G * kHeadDim + kAttnThreads - 1) / kAttnThreads;
+        float part[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int e = tid + j * kAttnThreads;
+            part[j] = 0.0f;
+            if (e < G * kHeadDim) {
+                const int h = e / kHeadDim, d = e % kHeadDim;
+#pragma unroll
+                for (int w = 0; w < kAttnWarps; ++w)
+                    part[j] += sm_o[w][h][d] * sm_w[w][h];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int e = tid + j * kAttnThreads;
+            if (e < G * kHeadDim)
+                sm_o[0][e / kHeadDim][e % kHeadDim] = part[j];
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();  // every split's partial is in its shared memory
+        if (split == 0) {
+            const int ns = (int)cluster.num_blocks();
+            __shared__ float sm_cw[kMaxClusterSplits][G];  // merge weight of split r, head h
+            if (tid < G) {
+                float M = -CUDART_INF_F;
+                for (int r = 0; r < ns; ++r)
+                    M = fmaxf(M, *cluster.map_shared_rank(&sm_M[tid], r));
+                float L = 0.0f;
+                for (int r = 0; r < ns; ++r) {
+                    const float wt = safe_exp2_diff(*cluster.map_shared_rank(&sm_M[tid], r), M);
+                    sm_cw[r][tid] = wt;
+                    L += *cluster.map_shared_rank(&sm_L[tid], r) * wt;
+                }
+                sm_red[0][tid] = L;
+            }
+            __syncthreads();
+            for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
+                const int h = e / kHeadDim, d = e % kHeadDim;
+                float acc = 0.0f;
+                for (int r = 0; r < ns; ++r)
+                    acc += sm_cw[r][h] * *cluster.map_shared_rank(&sm_o[0][h][d], r);
+                const float L = sm_red[0][h];
+                const float val = L > 0.0f ? acc / L : 0.0f;
+                a.out[(out_row0 + h) * kHeadDim + d] = f32_to_bf16_rn(val);
+                if (a.out_f32)
+                    a.out_f32[(out_row0 + h) * kHeadDim + d] = val;
+            }
+        }
+        cluster.sync();  // keep every split's shared memory alive until split 0 has read it
+        return;
+    }
     if (nsplit_b == 1) {
         for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
             const int h = e / kHeadDim, d = e % kHeadDim;
@@ -435,27 +525,46 @@ attention_kernel(const AttnArgs a)
         a.tickets[bg] = 0u;  // ready for the next launch on this workspace
 }
 
-template <int G, bool SPARSE, bool SELECT>
+int g_carveout = -1;  // preferred shared-memory carveout (percent) for the attention kernels
+
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER>
 cudaError_t launch_one(const AttnArgs &a, int batch, cudaStream_t stream)
 {
+    if (g_carveout >= 0)
+        cudaFuncSetAttribute(attention_kernel<G, SPARSE, SELECT, CLUSTER>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, g_carveout);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.nsplit, (unsigned)a.Hkv, (unsigned)batch);
     cfg.blockDim = dim3(kAttnThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int nattr = 1;
+    if (CLUSTER) {
+        if (a.nsplit > 8) {  // beyond the portable cluster size
+            cudaError_t e = cudaFuncSetAttribute(attention_kernel<G, SPARSE, SELECT, CLUSTER>,
+                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess)
+                return e;
+        }
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)a.nsplit;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        nattr = 2;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attention_kernel<G, SPARSE, SELECT>, a);
+    cfg.numAttrs = nattr;
+    return cudaLaunchKernelEx(&cfg, attention_kernel<G, SPARSE, SELECT, CLUSTER>, a);
 }
 
 template <int G, bool SPARSE, bool SELECT>
 int occupancy_one()
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<G, SPARSE, SELECT>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<G, SPARSE, SELECT, false>,
                                                       kAttnThreads, 0) != cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
@@ -463,16 +572,21 @@ int occupancy_one()
 
 }  // namespace
 
-cudaError_t launch_attention(int G, bool sparse, bool select, const AttnArgs &a, int batch,
-                             cudaStream_t stream)
+void set_attention_carveout(int percent) { g_carveout = percent; }
+
+cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, const AttnArgs &a,
+                             int batch, cudaStream_t stream)
 {
-#define TD_DISPATCH_G(GG)                                                 \
-    case GG:                                                              \
-        if (sparse)                                                       \
-            return launch_one<GG, true, false>(a, batch, stream);         \
-        if (select)                                                       \
-            return launch_one<GG, false, true>(a, batch, stream);         \
-        return launch_one<GG, false, false>(a, batch, stream);
+#define TD_DISPATCH_G(GG)                                                             \
+    case GG:                                                                          \
+        if (sparse)                                                                   \
+            return cluster ? launch_one<GG, true, false, true>(a, batch, stream)      \
+                           : launch_one<GG, true, false, false>(a, batch, stream);    \
+        if (select)                                                                   \
+            return cluster ? launch_one<GG, false, true, true>(a, batch, stream)      \
+                           : launch_one<GG, false, true, false>(a, batch, stream);    \
+        return cluster ? launch_one<GG, false, false, true>(a, batch, stream)         \
+                       : launch_one<GG, false, false, false>(a, batch, stream);
     switch (G) {
         TD_DISPATCH_G(1)
         TD_DISPATCH_G(2)

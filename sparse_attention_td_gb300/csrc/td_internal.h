@@ -15,11 +15,16 @@ constexpr int kTokPerHalf = 4;         // tokens a half-warp handles per round
 constexpr int kTokPerRound = kAttnWarps * 2 * kTokPerHalf;  // 64 tokens per CTA round
 constexpr int kChunkGranule = 16;      // split lengths are multiples of this many tokens
 constexpr int kMaxSplits = 256;        // splits per (batch, KV head)
+constexpr int kMaxClusterSplits = 16;  // splits a cluster merge can take (non-portable above 8)
+constexpr int kPortableClusterSplits = 8;  // the split counts merged through a cluster by default
 constexpr int kMaxSplitCtas = 8192;    // cap on batch * kv_heads * splits for partials
 constexpr int kMaxSparseChunk = 2048;  // index entries one sparse CTA stages in shared memory
 constexpr int kMaxTopK = kMaxSplits * kMaxSparseChunk;
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkCandidates = 16384;  // (key, position) pairs a top-k CTA holds in shared memory
+constexpr int kSelectBits = 11;         // first radix digit of the top-k select (key bits 31..21)
+constexpr int kSelectBins = 1 << kSelectBits;
+constexpr int kTopkBitmapBits = 1 << 18; // rows up to this length are compacted through a bitmap
 
 constexpr uint32_t kFlagIndexOutOfRange = 0x1u;
 constexpr uint32_t kFlagSeqLenOutOfRange = 0x2u;
@@ -35,6 +40,7 @@ struct AttnArgs {
     uint16_t *out;           // [B][Hq][128]
     float *out_f32;          // optional
     float *scores;           // select: [B][Hkv][Nmax]
+    unsigned *hist;          // select: [B*Hkv][kSelectBins] first-digit histogram (zero on entry)
     float *part_m;           // [B*Hkv][nsplit][G]  running max (log2 units)
     float *part_l;           // [B*Hkv][nsplit][G]  softmax denominator
     float *part_o;           // [B*Hkv][nsplit][G][128] un-normalised output
@@ -49,6 +55,7 @@ struct AttnArgs {
 
 struct TopkArgs {
     const float *scores;     // [B][Hkv][Nmax]
+    unsigned *hist;          // [B*Hkv][kSelectBins] from the attention kernel, or null; zeroed after use
     const int32_t *seq_lens; // [B]
     int32_t *idx;            // [B][Hkv][top_k]
     uint32_t *status;
@@ -56,9 +63,14 @@ struct TopkArgs {
 };
 
 // G = query heads per KV head (1, 2, 4, 8).
-cudaError_t launch_attention(int G, bool sparse, bool select, const AttnArgs &a, int batch,
-                             cudaStream_t stream);
+// cluster: merge the splits through a thread-block cluster (requires
+// a.nsplit <= kMaxClusterSplits); otherwise through global partials.
+cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, const AttnArgs &a,
+                             int batch, cudaStream_t stream);
 cudaError_t launch_topk(const TopkArgs &a, int batch, cudaStream_t stream);
+
+// Preferred shared-memory carveout (percent, -1 = driver default) for later attention launches.
+void set_attention_carveout(int percent);
 
 // Resident CTAs per SM of one attention instantiation (occupancy query).
 int attention_ctas_per_sm(int G, bool sparse, bool select);

@@ -9,19 +9,22 @@
 // ascending position order and padded with -1 when seq_lens[b] < k.
 //
 // Method: exact radix select on order-preserving 32-bit keys, one 1024-thread
-// CTA per row, three reads of the row:
+// CTA per row:
 //   1. an 11-bit histogram of the keys' top bits picks the bin holding the
-//      k-th largest key;
-//   2. that bin's (key, position) pairs are gathered into shared memory and
-//      the select finishes there: the k-th key T, and -- when only some of
-//      the keys equal to T fit in the set -- the largest position P that
-//      still does (the lowest positions win ties);
-//   3. an ordered compaction keeps every key > T and every key == T at a
-//      position <= P, with ballot-based block scans assigning output slots
-//      in position order.
-// Loads are batched eight per thread so each thread keeps eight in flight.
-// If the threshold bin is larger than the shared-memory buffer (heavily tied
-// scores), the remaining digits are selected by streaming passes instead.
+//      k-th largest key.  In a selection layer the attention kernel that
+//      wrote the scores already built it (and this kernel clears it again);
+//      for caller-given scores it is counted here.
+//   2. One read of the row: keys above that bin are marked in a shared-memory
+//      bitmap of the row's positions, and the bin's (key, position) pairs
+//      are gathered into shared memory.  The select finishes on the gathered
+//      pairs (in one warp when there are few): the k-th key T and, when only
+//      some keys equal to T fit in the set, the largest position P that still
+//      does (the lowest positions win ties).  The selected pairs are marked.
+//   3. The set is written in position order by a block-wide scan of the
+//      bitmap.
+// Loads are batched sixteen per thread.  Rows longer than the bitmap, or a
+// threshold bin larger than the shared-memory buffer (heavily tied scores),
+// fall back to streaming passes and an ordered compaction of the row.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,9 +36,12 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kT = kTopkThreads;        // 1024
 constexpr int kWarps = kT / 32;         // 32
-constexpr int kBatch = 8;               // loads in flight per thread
-constexpr int kBits1 = 11;              // first digit: key bits 31..21
-constexpr int kBins1 = 1 << kBits1;     // 2048
+constexpr int kBatch = 16;              // loads in flight per thread
+constexpr unsigned kWarpSelectMax = 2048; // threshold bins up to this size finish in one warp
+constexpr int kBits1 = kSelectBits;     // first digit: key bits 31..21
+constexpr int kBins1 = kSelectBins;     // 2048
+constexpr int kBitmapWords = kTopkBitmapBits / 32;
+constexpr int kWordsPerThread = kBitmapWords / kT;
 constexpr int kSubHists = 4;            // pass-1 sub-histograms (less atomic contention)
 
 // Programmatic dependent launch (see td_attn.cu): the scores come from the
@@ -68,6 +74,7 @@ struct TopkSmem {
     unsigned pre[kBatch * kWarps];
     unsigned res[2];                    // digit, remaining rank
     unsigned cand_count;
+    unsigned bitmap[kBitmapWords];      // selected positions of rows up to kTopkBitmapBits long
 };
 
 // Block-wide search over a histogram of NB bins (digit = bin index): the
@@ -117,6 +124,38 @@ __device__ void find_digit(TopkSmem &sm, const unsigned *hist, unsigned r)
         }
     }
     __syncthreads();
+}
+
+// Exclusive prefix sum of v over the block (thread order); *total gets the sum.
+__device__ __forceinline__ unsigned block_exclusive_sum(TopkSmem &sm, unsigned v, unsigned *total)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned incl = v;
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned t = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off)
+            incl += t;
+    }
+    if (lane == 31)
+        sm.scan[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const unsigned w = sm.scan[lane];
+        unsigned wi = w;
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned t = __shfl_up_sync(kFull, wi, off);
+            if (lane >= off)
+                wi += t;
+        }
+        sm.scan[lane] = wi - w;
+        if (lane == 31)
+            sm.res[0] = wi;
+    }
+    __syncthreads();
+    const unsigned excl = incl - v + sm.scan[warp];
+    *total = sm.res[0];
+    __syncthreads();
+    return excl;
 }
 
 // Calls f(key, pos) for every position of the row, eight loads in flight per thread.
@@ -176,6 +215,74 @@ __device__ uint32_t radix_select(TopkSmem &sm, Src src, int hi_bit, uint32_t pre
     return prefix;
 }
 
+// One warp's radix select over n items of a shared-memory list: the r-th
+// largest value val(i) among the items with keep(i), digits of 8 bits over
+// bits [hi_bit..0] below the already fixed `prefix`/`mask`.  `hist` is a
+// 256-bin scratch histogram private to the warp.  Returns the value;
+// *rank_out = how many items equal to it belong in the set, *eq_out = how
+// many items equal it.  Warp-synchronous: no block barrier.
+template <class ValF, class KeepF>
+__device__ uint32_t warp_select(unsigned *hist, unsigned n, ValF val, KeepF keep, int hi_bit,
+                                uint32_t prefix, uint32_t mask, unsigned r, unsigned *rank_out,
+                                unsigned *eq_out)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned last = 0;
+    for (int top = hi_bit; top >= 0; top -= 8) {
+        const int width = top + 1 < 8 ? top + 1 : 8;
+        const int shift = top + 1 - width;
+        const unsigned dmask = (1u << width) - 1u;
+        for (int i = lane; i < 256; i += 32)
+            hist[i] = 0u;
+        __syncwarp();
+        for (unsigned i = lane; i < n; i += 32) {
+            if (!keep(i))
+                continue;
+            const uint32_t v = val(i);
+            if ((v & mask) == prefix)
+                atomicAdd(&hist[(v >> shift) & dmask], 1u);
+        }
+        __syncwarp();
+        // lane L owns bins 255-8L down to 248-8L; counts accumulate from the top
+        unsigned mine = 0;
+        for (int i = 0; i < 8; ++i)
+            mine += hist[255 - 8 * lane - i];
+        unsigned incl = mine;
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned t = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off)
+                incl += t;
+        }
+        const unsigned excl = incl - mine;
+        const bool owner = excl < r && r <= incl;
+        unsigned d = 0, rn = 0, cnt = 0;
+        if (owner) {
+            unsigned run = excl;
+            for (int i = 0; i < 8; ++i) {
+                const unsigned bin = 255 - 8 * lane - i;
+                const unsigned h = hist[bin];
+                if (run + h >= r) {
+                    d = bin;
+                    rn = r - run;
+                    cnt = h;
+                    break;
+                }
+                run += h;
+            }
+        }
+        const int src = __ffs(__ballot_sync(kFull, owner)) - 1;
+        d = __shfl_sync(kFull, d, src);
+        r = __shfl_sync(kFull, rn, src);
+        last = __shfl_sync(kFull, cnt, src);
+        prefix |= d << shift;
+        mask |= dmask << shift;
+        __syncwarp();
+    }
+    *rank_out = r;
+    *eq_out = last;
+    return prefix;
+}
+
 __global__ void __launch_bounds__(kTopkThreads, 1)
 topk_kernel(const TopkArgs a)
 {
@@ -199,28 +306,38 @@ topk_kernel(const TopkArgs a)
     pdl_wait();
     pdl_launch_dependents();
 
+    unsigned *ghist = a.hist ? a.hist + bg * kBins1 : nullptr;
     if (n <= k) {  // every position is kept
         for (int j = tid; j < k; j += kT)
             out[j] = j < n ? j : -1;
+        if (ghist)
+            for (int i = tid; i < kBins1; i += kT)
+                ghist[i] = 0u;  // leave the fused histogram zero for the next selection
         return;
     }
 
-    // 1. histogram of the top 11 bits
-    for (int i = tid; i < kSubHists * kBins1; i += kT)
-        sm.hist[i] = 0u;
+    // 1. histogram of the top 11 bits: from the attention kernel that wrote
+    //    the scores (then cleared for the next selection), else counted here
     if (tid == 0)
         sm.cand_count = 0u;
-    __syncthreads();
-    {
+    if (ghist) {
+        for (int i = tid; i < kBins1; i += kT) {
+            sm.hist[i] = __ldcg(&ghist[i]);
+            ghist[i] = 0u;
+        }
+    } else {
+        for (int i = tid; i < kSubHists * kBins1; i += kT)
+            sm.hist[i] = 0u;
+        __syncthreads();
         unsigned *mine = sm.hist + (warp % kSubHists) * kBins1;
         stream_row(s, n, [&](uint32_t key, int) { atomicAdd(&mine[key >> (32 - kBits1)], 1u); });
-    }
-    __syncthreads();
-    for (int i = tid; i < kBins1; i += kT) {
-        unsigned t = 0;
-        for (int h = 0; h < kSubHists; ++h)
-            t += sm.hist[h * kBins1 + i];
-        sm.hist[i] = t;
+        __syncthreads();
+        for (int i = tid; i < kBins1; i += kT) {
+            unsigned t = 0;
+            for (int h = 0; h < kSubHists; ++h)
+                t += sm.hist[h * kBins1 + i];
+            sm.hist[i] = t;
+        }
     }
     __syncthreads();
     find_digit<kBins1>(sm, sm.hist, (unsigned)k);
@@ -234,8 +351,15 @@ topk_kernel(const TopkArgs a)
     uint32_t T;
     unsigned need_eq, n_eq;
     int P = 0x7fffffff;  // largest kept position among keys == T
+    const bool use_bitmap = n <= kTopkBitmapBits;
     if (bin_count <= (unsigned)kTopkCandidates) {
-        // 2. gather the threshold bin into shared memory, finish there
+        // 2. gather the threshold bin into shared memory, finish there; rows
+        //    that fit the bitmap also mark every key above the bin as selected
+        if (use_bitmap) {
+            for (int w = tid; w < (n + 31) / 32; w += kT)
+                sm.bitmap[w] = 0u;
+            __syncthreads();
+        }
         for (int base = 0; base < n; base += kT * kBatch) {
             float v[kBatch];
 #pragma unroll
@@ -248,6 +372,12 @@ topk_kernel(const TopkArgs a)
                 const int i = base + j * kT + tid;
                 const uint32_t key = order_key(v[j]);
                 const bool hit = i < n && (key & mask1) == prefix1;
+                if (use_bitmap) {
+                    // a warp covers one aligned 32-position word: store it whole
+                    const unsigned above = __ballot_sync(kFull, i < n && key > (prefix1 | ~mask1));
+                    if (lane == 0 && i < n)
+                        sm.bitmap[i >> 5] = above;
+                }
                 const unsigned m = __ballot_sync(kFull, hit);
                 if (m) {  // warp-uniform
                     unsigned slot0 = 0;
@@ -264,6 +394,30 @@ topk_kernel(const TopkArgs a)
         }
         __syncthreads();
         const unsigned cnt = sm.cand_count;
+        if (use_bitmap && cnt <= kWarpSelectMax) {
+            // small threshold bin: one warp finishes the select and marks the
+            // selected candidates, without block-wide barriers
+            if (warp == 0) {
+                unsigned need, neq;
+                const uint32_t t = warp_select(
+                    sm.hist, cnt, [&](unsigned i) { return cand_key[i]; },
+                    [&](unsigned) { return true; }, 31 - kBits1, prefix1, mask1, r1, &need, &neq);
+                int p_cut = 0x7fffffff;
+                if (need < neq) {
+                    unsigned r2, e2;
+                    p_cut = (int)~warp_select(
+                        sm.hist, cnt, [&](unsigned i) { return ~(uint32_t)cand_pos[i]; },
+                        [&](unsigned i) { return cand_key[i] == t; }, 31, 0u, 0u, need, &r2, &e2);
+                }
+                for (unsigned i = lane; i < cnt; i += 32) {
+                    const uint32_t key = cand_key[i];
+                    const int pos = cand_pos[i];
+                    if (key > t || (key == t && pos <= p_cut))
+                        atomicOr(&sm.bitmap[pos >> 5], 1u << (pos & 31));
+                }
+            }
+            __syncthreads();
+        } else {
         auto cand_src = [&](auto f) {
             for (unsigned i = tid; i < cnt; i += kT)
                 f(cand_key[i], cand_pos[i]);
@@ -278,6 +432,43 @@ topk_kernel(const TopkArgs a)
             };
             unsigned r_dummy, e_dummy;
             P = (int)~radix_select(sm, eq_src, 31, 0u, 0u, need_eq, &r_dummy, &e_dummy);
+        }
+        if (use_bitmap) {
+            // mark the selected part of the threshold bin
+            for (unsigned i = tid; i < cnt; i += kT) {
+                const uint32_t key = cand_key[i];
+                const int pos = cand_pos[i];
+                if (key > T || (key == T && pos <= P))
+                    atomicOr(&sm.bitmap[pos >> 5], 1u << (pos & 31));
+            }
+            __syncthreads();
+        }
+        }  // large threshold bin
+        if (use_bitmap) {
+            // write the set in position order by scanning the bitmap (no second row read)
+            const int words = (n + 31) / 32;
+            unsigned w[kWordsPerThread];
+            unsigned count = 0;
+#pragma unroll
+            for (int j = 0; j < kWordsPerThread; ++j) {
+                const int wi = tid * kWordsPerThread + j;
+                w[j] = wi < words ? sm.bitmap[wi] : 0u;
+                count += __popc(w[j]);
+            }
+            unsigned total;
+            unsigned slot = block_exclusive_sum(sm, count, &total);
+#pragma unroll
+            for (int j = 0; j < kWordsPerThread; ++j) {
+                unsigned word = w[j];
+                while (word) {
+                    const int bit = __ffs(word) - 1;
+                    word &= word - 1u;
+                    if (slot < (unsigned)k)  // exactly k bits are set; the bound only guards memory
+                        out[slot] = (tid * kWordsPerThread + j) * 32 + bit;
+                    ++slot;
+                }
+            }
+            return;
         }
     } else {
         // threshold bin too large for shared memory: stream the remaining digits
@@ -318,10 +509,11 @@ topk_kernel(const TopkArgs a)
         __syncthreads();
         if (warp == 0) {
             // exclusive scan of the 256 counts in (j, warp) order = position order
-            unsigned c[8], sum = 0;
+            constexpr int per = kBatch * kWarps / 32;  // counts per lane, position order
+            unsigned c[per], sum = 0;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                c[e] = sm.tot[lane * 8 + e];
+            for (int e = 0; e < per; ++e) {
+                c[e] = sm.tot[lane * per + e];
                 sum += c[e];
             }
             unsigned incl = sum;
@@ -332,8 +524,8 @@ topk_kernel(const TopkArgs a)
             }
             unsigned run = incl - sum;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                sm.pre[lane * 8 + e] = run;
+            for (int e = 0; e < per; ++e) {
+                sm.pre[lane * per + e] = run;
                 run += c[e];
             }
             if (lane == 31)

@@ -349,3 +349,33 @@ def test_sparse_before_selection_launches_nothing():
     td.td_decode_step(shape, [td.MODE_FULL, td.MODE_SPARSE], [x, x], [kv, kv], [kv, kv], seq, 4,
                       idx, [x.clone(), x.clone()], None, ws, idx_valid=True)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_cluster_and_global_split_merges_agree(orc, sparse):
+    """The splits of a (batch, KV head) merge either through a thread-block
+    cluster or through global partials and a ticket; both match the oracle."""
+    G, Hkv, B, N = 4, 2, 3, 3000
+    lens = [3000, 1111, 70]
+    shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
+    q, K, V, _ = W.random_case(50 + sparse, B, G * Hkv, Hkv, N, lens)
+    idx = W.random_index_sets(52, B, Hkv, 900, lens, pad_fraction=0.05)
+    res = {}
+    try:
+        for mode in (1, -1):
+            td.td_set_tuning("cluster", mode)
+            td.td_set_tuning("max_splits", 12)
+            if sparse:
+                out, out32, st = run_sparse(shape, q, K, V, lens, idx, 900)
+                assert st == 0
+            else:
+                out, out32, _, _ = run_full(shape, q, K, V, lens)
+            res[mode] = (out, out32)
+    finally:
+        td.td_set_tuning("cluster", 0)
+        td.td_set_tuning("max_splits", 0)
+    ref = oracle_sparse(orc, shape, q, K, V, idx) if sparse else oracle_full(orc, shape, q, K, V, lens)
+    for mode, (out, out32) in res.items():
+        check_outputs(out, out32, ref, f"merge mode {mode}")
+    rowmax = res[-1][1].abs().amax(dim=-1, keepdim=True).clamp_min(1e-6)
+    assert ((res[1][1] - res[-1][1]).abs() / rowmax).max().item() <= 2e-6
