@@ -453,69 +453,45 @@ attention_kernel(const AttnArgs a)
         return;
     __threadfence();
 
-    // Last CTA of this (batch, KV head): merge all splits.
+    // Last CTA of this (batch, KV head): merge all splits.  Each output
+    // element's thread reads every split's (m, l) of its head and its own o
+    // values as one batch of independent loads (chunks of kMergeChunk splits),
+    // then reduces locally: one round trip instead of three with barriers.
     const size_t pb0 = bg * (size_t)a.nsplit * G;
-    float mx[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-        mx[h] = -CUDART_INF_F;
-    for (int s = tid; s < nsplit_b; s += kAttnThreads)
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-            mx[h] = fmaxf(mx[h], __ldcg(&a.part_m[pb0 + (size_t)s * G + h]));
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], off));
-        if (lane == 0)
-            sm_red[warp][h] = mx[h];
-    }
-    __syncthreads();
-    if (tid < G) {
-        float M = -CUDART_INF_F;
-        for (int w = 0; w < kAttnWarps; ++w)
-            M = fmaxf(M, sm_red[w][tid]);
-        sm_M[tid] = M;
-    }
-    __syncthreads();
-    float ls[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-        ls[h] = 0.0f;
-    for (int s = tid; s < nsplit_b; s += kAttnThreads)
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float wt = safe_exp2_diff(__ldcg(&a.part_m[pb0 + (size_t)s * G + h]), sm_M[h]);
-            sm_sw[s * G + h] = wt;
-            ls[h] += __ldcg(&a.part_l[pb0 + (size_t)s * G + h]) * wt;
-        }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-            ls[h] += __shfl_xor_sync(kFull, ls[h], off);
-    }
-    __syncthreads();  // sm_red reuse
-    if (lane == 0)
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-            sm_red[warp][h] = ls[h];
-    __syncthreads();
-    if (tid < G) {
-        float L = 0.0f;
-        for (int w = 0; w < kAttnWarps; ++w)
-            L += sm_red[w][tid];
-        sm_L[tid] = L;
-    }
-    __syncthreads();
+    constexpr int kMergeChunk = 16;
     for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
         const int h = e / kHeadDim, d = e % kHeadDim;
-        float acc = 0.0f;
-#pragma unroll 4
-        for (int s = 0; s < nsplit_b; ++s)
-            acc += sm_sw[s * G + h] * __ldcg(&a.part_o[(pb0 + (size_t)s * G + h) * kHeadDim + d]);
-        const float L = sm_L[h];
+        float M = -CUDART_INF_F, L = 0.0f, acc = 0.0f;
+        for (int s0 = 0; s0 < nsplit_b; s0 += kMergeChunk) {
+            float mv[kMergeChunk], lv[kMergeChunk], ov[kMergeChunk];
+#pragma unroll
+            for (int j = 0; j < kMergeChunk; ++j) {
+                const int s = s0 + j;
+                mv[j] = -CUDART_INF_F;
+                lv[j] = 0.0f;
+                ov[j] = 0.0f;
+                if (s < nsplit_b) {
+                    const size_t ps = pb0 + (size_t)s * G + h;
+                    mv[j] = __ldcg(&a.part_m[ps]);
+                    lv[j] = __ldcg(&a.part_l[ps]);
+                    ov[j] = __ldcg(&a.part_o[ps * kHeadDim + d]);
+                }
+            }
+            float Mc = M;
+#pragma unroll
+            for (int j = 0; j < kMergeChunk; ++j)
+                Mc = fmaxf(Mc, mv[j]);
+            const float r = safe_exp2_diff(M, Mc);  // rescale what earlier chunks added
+            acc *= r;
+            L *= r;
+#pragma unroll
+            for (int j = 0; j < kMergeChunk; ++j) {
+                const float wt = safe_exp2_diff(mv[j], Mc);
+                acc += wt * ov[j];
+                L += wt * lv[j];
+            }
+            M = Mc;
+        }
         const float val = L > 0.0f ? acc / L : 0.0f;
         a.out[(out_row0 + h) * kHeadDim + d] = f32_to_bf16_rn(val);
         if (a.out_f32)

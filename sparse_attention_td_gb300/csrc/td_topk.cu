@@ -22,7 +22,8 @@
 //      does (the lowest positions win ties).  The selected pairs are marked.
 //   3. The set is written in position order by a block-wide scan of the
 //      bitmap.
-// Loads are batched sixteen per thread.  Rows longer than the bitmap, or a
+// Loads are batched sixteen scores per thread (four float4 loads on 16-byte
+// aligned rows).  Rows longer than the bitmap, or a
 // threshold bin larger than the shared-memory buffer (heavily tied scores),
 // fall back to streaming passes and an ordered compaction of the row.
 #include <cuda_runtime.h>
@@ -37,6 +38,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kT = kTopkThreads;        // 1024
 constexpr int kWarps = kT / 32;         // 32
 constexpr int kBatch = 16;              // loads in flight per thread
+constexpr int kBatchV = 4;              // float4 loads in flight per thread (16 scores)
 constexpr unsigned kWarpSelectMax = 2048; // threshold bins up to this size finish in one warp
 constexpr int kBits1 = kSelectBits;     // first digit: key bits 31..21
 constexpr int kBins1 = kSelectBins;     // 2048
@@ -360,7 +362,68 @@ topk_kernel(const TopkArgs a)
                 sm.bitmap[w] = 0u;
             __syncthreads();
         }
-        for (int base = 0; base < n; base += kT * kBatch) {
+        const uint32_t top_of_bin = prefix1 | ~mask1;  // largest key inside the threshold bin
+        const int vec_n = (((uintptr_t)s & 15u) == 0) ? n / 4 : 0;  // whole float4 groups
+        // Aligned rows: a thread takes 4 consecutive scores per load, so a warp
+        // covers 128 positions = 4 bitmap words (a word's 8 nibbles are OR-ed
+        // together with 3 shuffles) and appends its candidates after one warp scan.
+        for (int base = 0; base < vec_n; base += kT * kBatchV) {
+            float4 v[kBatchV];
+#pragma unroll
+            for (int j = 0; j < kBatchV; ++j) {
+                const int i4 = base + j * kT + tid;
+                v[j] = i4 < vec_n ? __ldcg(reinterpret_cast<const float4 *>(s) + i4)
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int j = 0; j < kBatchV; ++j) {
+                const int i4 = base + j * kT + tid;
+                const int pos0 = 4 * i4;
+                const bool live = i4 < vec_n;
+                const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                uint32_t key[4];
+                unsigned hitm = 0u, abovem = 0u;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    key[e] = order_key(f[e]);
+                    hitm |= (live && (key[e] & mask1) == prefix1) ? (1u << e) : 0u;
+                    abovem |= (live && key[e] > top_of_bin) ? (1u << e) : 0u;
+                }
+                if (use_bitmap) {
+                    unsigned word = abovem << (4 * (lane & 7));
+                    word |= __shfl_xor_sync(kFull, word, 1);
+                    word |= __shfl_xor_sync(kFull, word, 2);
+                    word |= __shfl_xor_sync(kFull, word, 4);
+                    if ((lane & 7) == 0 && live)
+                        sm.bitmap[pos0 >> 5] = word;
+                }
+                const unsigned cnt = __popc(hitm);
+                unsigned incl = cnt;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const unsigned t = __shfl_up_sync(kFull, incl, off);
+                    if (lane >= off)
+                        incl += t;
+                }
+                const unsigned total = __shfl_sync(kFull, incl, 31);
+                if (total) {  // warp-uniform
+                    unsigned slot0 = 0;
+                    if (lane == 0)
+                        slot0 = atomicAdd(&sm.cand_count, total);
+                    unsigned slot = __shfl_sync(kFull, slot0, 0) + incl - cnt;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (hitm & (1u << e)) {
+                            cand_key[slot] = key[e];
+                            cand_pos[slot] = pos0 + e;
+                            ++slot;
+                        }
+                }
+            }
+        }
+        __syncthreads();  // whole-word bitmap stores above land before the tail ORs into a word
+        // the rest (unaligned rows, or the tail after the last whole group), one score per thread
+        for (int base = 4 * vec_n; base < n; base += kT * kBatch) {
             float v[kBatch];
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
@@ -372,12 +435,8 @@ topk_kernel(const TopkArgs a)
                 const int i = base + j * kT + tid;
                 const uint32_t key = order_key(v[j]);
                 const bool hit = i < n && (key & mask1) == prefix1;
-                if (use_bitmap) {
-                    // a warp covers one aligned 32-position word: store it whole
-                    const unsigned above = __ballot_sync(kFull, i < n && key > (prefix1 | ~mask1));
-                    if (lane == 0 && i < n)
-                        sm.bitmap[i >> 5] = above;
-                }
+                if (use_bitmap && i < n && key > top_of_bin)  // may share a word with the vector part
+                    atomicOr(&sm.bitmap[i >> 5], 1u << (i & 31));
                 const unsigned m = __ballot_sync(kFull, hit);
                 if (m) {  // warp-uniform
                     unsigned slot0 = 0;
