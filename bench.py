@@ -208,16 +208,16 @@ def attn_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes per launch of the full-attention kernel from a committed ncu
-    summary, or None if there is none for this workload or the kernel source
-    changed since it was taken."""
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of one attention kernel ("full" or "sparse") from
+    a committed ncu summary, or None if there is none for this workload or the
+    kernel source changed since it was taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    entry = rec.get(workload)
+    entry = rec.get(f"{workload}:{kernel}")
     if not entry or entry.get("source_hash") != attn_source_hash():
         return None
     return entry.get("dram_bytes_per_launch")
@@ -348,11 +348,36 @@ def run_ours(args, world, rank, local):
     bytes_model = step_bytes(wl, lens, modes)
     peaks, peak_kind = load_measured_peaks()
     peak = float(peaks["hbm_gbs"])
+    # Roofline of each attention kernel from the traced pass: algorithmic bytes
+    # of one launch / its mean layer time.  The full kernel's launches are the
+    # full layers (full+select layers add the top-k kernel to the layer time).
+    # The step's dominant kernel is the one with the most time in the step.
+    counts = {name: sum(1 for m in modes if m == mm)
+              for name, mm in (("full", W.FULL), ("full_select", W.FULL_SELECT),
+                               ("sparse", W.SPARSE))}
+    step_sum = sum(by_mode[k] * counts[k] for k in by_mode)
+    kernels = {}
     full_launch_us = by_mode.get("full", by_mode.get("full_select"))
-    achieved = bytes_model["per_launch"]["full"] / (full_launch_us * 1e-6) / 1e9
-    sparse_gbs = (bytes_model["per_launch"]["sparse"] / (by_mode["sparse"] * 1e-6) / 1e9
-                  if "sparse" in by_mode else None)
-    traffic = measured_traffic(wl.name)
+    kernels["full"] = {
+        "kernel": "attention_kernel<G,full> (split-K flash decode over all N_b tokens + combine)",
+        "launch_us": full_launch_us, "bytes": bytes_model["per_launch"]["full"],
+        "share": (full_launch_us * (counts["full"] + counts["full_select"])) / step_sum}
+    if "sparse" in by_mode:
+        kernels["sparse"] = {
+            "kernel": "attention_kernel<G,sparse> (gather of the k persisted K/V rows + combine)",
+            "launch_us": by_mode["sparse"], "bytes": bytes_model["per_launch"]["sparse"],
+            "share": by_mode["sparse"] * counts["sparse"] / step_sum}
+    rooflines = {}
+    for name, kk in kernels.items():
+        ach = kk["bytes"] / (kk["launch_us"] * 1e-6) / 1e9
+        rooflines[name] = {
+            "kernel": kk["kernel"], "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(ach / peak, 4),
+            "traffic": measured_traffic(wl.name, name), "peak_source": f"{peak_kind} hbm_gbs",
+            "algorithmic_bytes_per_launch": kk["bytes"], "launch_us": round(kk["launch_us"], 2),
+            "share_of_traced_step": round(kk["share"], 4)}
+    dominant = max(kernels, key=lambda k: kernels[k]["share"])
+    sparse_gbs = rooflines["sparse"]["achieved"] if "sparse" in rooflines else None
     launches_per_step = sum(2 if m == W.FULL_SELECT else 1 for m in modes)
 
     result = None
@@ -389,14 +414,8 @@ def run_ours(args, world, rank, local):
             "traced_step_us": round(traced_step_us, 2),
             "layer_us": {k: round(v, 2) for k, v in by_mode.items()},
             "sparse_layer_gbs": round(sparse_gbs, 1) if sparse_gbs else None,
-            "roofline": {
-                "kernel": "attention_kernel<G,full> (full layer: split-K flash decode + combine)",
-                "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                "algorithmic_bytes_per_launch": bytes_model["per_launch"]["full"],
-                "launch_us": round(full_launch_us, 2),
-            },
+            "roofline": rooflines[dominant],
+            "rooflines": rooflines,
             "gpu_launches": launches_per_step * K_steps,
             "e2e": {"value": round(e2e_us, 2), "unit": "us", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

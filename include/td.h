@@ -69,6 +69,8 @@ typedef enum {
 /* Bits of the device status word (td_workspace_status). */
 #define TD_FLAG_INDEX_OUT_OF_RANGE 0x1u   /* idx entry < -1 or >= seq_lens[b]: skipped */
 #define TD_FLAG_SEQ_LEN_OUT_OF_RANGE 0x2u /* seq_lens[b] < 0 or > max_seq_len: clamped */
+#define TD_FLAG_WAIT_TIMEOUT 0x4u         /* a staged kernel's bounded wait for its copies gave up;
+                                             that (batch, KV head)'s output is not written */
 
 typedef struct {
     int32_t batch;          /* B  >= 1                                         */
@@ -227,7 +229,18 @@ void td_plan_destroy(td_plan *plan);
  *              thread-block cluster; 0 (default) through global partials
  *   "attn_carveout": preferred shared-memory carveout of the attention kernels
  *                    in percent (0..100; negative = driver default)
- * value <= 0 restores the default.  Unknown key -> TD_ERR_INVALID_ARG.
+ *   "full_staged": 1 stages the K/V rows of full (and full+select) layers
+ *                  through a ring of shared-memory stages filled by bulk
+ *                  asynchronous copies; 0 streams them straight into
+ *                  registers; negative restores the default (staged when
+ *                  num_q_heads / num_kv_heads >= 4)
+ *   "sparse_staged": 1 stages the gathered rows of sparse layers through a
+ *                  per-thread cp.async ring in shared memory; 0 (default) or
+ *                  negative streams them into registers
+ *   "topk_threads": 1024 or 512 threads per top-k row; other values restore
+ *                   the default (1024 when batch * kv_heads fits one wave of
+ *                   one CTA per SM, else 512 with two CTAs per SM)
+ * Otherwise value <= 0 restores the default.  Unknown key -> TD_ERR_INVALID_ARG.
  */
 td_status td_set_tuning(const char *key, int32_t value);
 

@@ -12,6 +12,7 @@ MODE_FULL_SELECT = 1
 MODE_SPARSE = 2
 FLAG_INDEX_OUT_OF_RANGE = 0x1
 FLAG_SEQ_LEN_OUT_OF_RANGE = 0x2
+FLAG_WAIT_TIMEOUT = 0x4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 

@@ -29,9 +29,23 @@ struct Tuning {
     int sparse_waves = 1;
     int max_splits = td::kMaxSplits;
     int cluster = 0;             // 1: merge up to kPortableClusterSplits splits through a cluster
+    int topk_threads = 0;        // 0 = by row count, else 512 or 1024
+    int full_staged = -1;        // 1: full / full+select kernels stage K/V through shared memory
+                                 // (bulk copies); 0: register-streamed; -1: staged when G >= 4
+    int sparse_staged = 0;       // 1: sparse kernels stage the gathered rows through shared memory
+                                 // (per-thread cp.async ring); 0: register-streamed
 };
 Tuning g_tuning;
 const Tuning kDefaultTuning;
+
+// Measured on GB300: staging pays for the grouped-query full kernels (G >= 4,
+// issue-bound at two CTAs per SM) and for none of the others.
+bool staged_for(bool sparse, int G)
+{
+    if (sparse)
+        return g_tuning.sparse_staged > 0;
+    return g_tuning.full_staged < 0 ? G >= 4 : g_tuning.full_staged > 0;
+}
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
@@ -164,7 +178,7 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
     const long units = (long)s.batch * s.num_kv_heads;
     int per_sm = sparse ? g_tuning.sparse_ctas_per_sm : g_tuning.full_ctas_per_sm;
     if (per_sm <= 0)
-        per_sm = td::attention_ctas_per_sm(G, sparse, select);
+        per_sm = td::attention_ctas_per_sm(G, sparse, select, staged_for(sparse, G));
     const long slots = (long)device_sm_count() * per_sm;  // resident CTAs per wave
     int waves = sparse ? g_tuning.sparse_waves : g_tuning.full_waves;
     if (waves <= 0)  // one wave of long CTAs when the pairs are few; more, shorter
@@ -261,7 +275,8 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
     a.hist = select ? (unsigned *)(c.wsb + c.ws.hist) : nullptr;
     plan_splits(c.shape, c.shape.max_seq_len, false, select, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
-    if (td::launch_attention(c.G, false, select, cluster, a, c.shape.batch, st) != cudaSuccess)
+    if (td::launch_attention(c.G, false, select, cluster, staged_for(false, c.G), a, c.shape.batch, st) !=
+        cudaSuccess)
         return TD_ERR_CUDA;
     if (select) {
         td::TopkArgs t{};
@@ -273,7 +288,7 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
         t.Hkv = c.shape.num_kv_heads;
         t.Nmax = c.shape.max_seq_len;
         t.top_k = top_k;
-        if (td::launch_topk(t, c.shape.batch, st) != cudaSuccess)
+        if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, st) != cudaSuccess)
             return TD_ERR_CUDA;
     }
     return TD_OK;
@@ -291,7 +306,8 @@ td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
     a.idx_dep = idx_dep ? 1 : 0;
     plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
-    if (td::launch_attention(c.G, true, false, cluster, a, c.shape.batch, st) != cudaSuccess)
+    if (td::launch_attention(c.G, true, false, cluster, staged_for(true, c.G), a, c.shape.batch, st) !=
+        cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }
@@ -464,7 +480,7 @@ td_status td_topk_select(const td_shape *shape, const float *scores, const int32
     t.Hkv = c.shape.num_kv_heads;
     t.Nmax = c.shape.max_seq_len;
     t.top_k = top_k;
-    if (td::launch_topk(t, c.shape.batch, (cudaStream_t)stream) != cudaSuccess)
+    if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, (cudaStream_t)stream) != cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }
@@ -593,6 +609,12 @@ td_status td_set_tuning(const char *key, int32_t value)
         g_tuning.sparse_waves = value > 0 ? value : kDefaultTuning.sparse_waves;
     else if (!strcmp(key, "cluster"))
         g_tuning.cluster = value > 0 ? 1 : 0;
+    else if (!strcmp(key, "full_staged"))
+        g_tuning.full_staged = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.full_staged);  // <0: auto
+    else if (!strcmp(key, "sparse_staged"))
+        g_tuning.sparse_staged = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.sparse_staged);
+    else if (!strcmp(key, "topk_threads"))
+        g_tuning.topk_threads = (value == 512 || value == 1024) ? value : 0;
     else if (!strcmp(key, "attn_carveout"))
         td::set_attention_carveout(value >= 0 && value <= 100 ? value : -1);
     else if (!strcmp(key, "max_splits"))

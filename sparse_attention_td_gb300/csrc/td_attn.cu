@@ -14,9 +14,16 @@
 // (an atomic ticket; nobody waits on anybody).
 //
 // The work is HBM-bound (about G flops per K/V byte), so there is no tensor
-// core path: each half-warp reads one 256-byte K row and one V row with
-// 16-byte loads (lane c holds dims 8c..8c+7), every thread keeps 4 tokens of
-// K and V in flight, and dot products are reduced with warp shuffles.
+// core path: each half-warp works on one 256-byte K row and one V row at a
+// time (lane c holds dims 8c..8c+7) and dot products are reduced with warp
+// shuffles.  The rows reach the registers one of two ways:
+//   * register-streamed: 16-byte loads straight from HBM, 4 tokens of K and V
+//     in flight per thread (32 KB per CTA);
+//   * staged: bulk asynchronous copies (the TMA engine's cp.async.bulk, one
+//     256-byte copy per gathered row, one copy per K or V block of contiguous
+//     rows) fill a ring of shared-memory stages of 64 tokens, completing on
+//     an mbarrier; the CTA computes on stage i while stages i+1.. are in
+//     flight (up to 128 KB per CTA).
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -32,16 +39,14 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // bf16 -> fp32 is exact: a bf16 value is the upper half of its fp32 word.
-__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8])
+// Pairs of consecutive dims as float2 (2j, 2j+1), for the packed fp32 pipe
+// (one fma.rn.f32x2 does two IEEE fmas).
+__device__ __forceinline__ void unpack8x2(const uint4 v, float2 (&f)[4])
 {
-    f[0] = __uint_as_float(v.x << 16);
-    f[1] = __uint_as_float(v.x & 0xffff0000u);
-    f[2] = __uint_as_float(v.y << 16);
-    f[3] = __uint_as_float(v.y & 0xffff0000u);
-    f[4] = __uint_as_float(v.z << 16);
-    f[5] = __uint_as_float(v.z & 0xffff0000u);
-    f[6] = __uint_as_float(v.w << 16);
-    f[7] = __uint_as_float(v.w & 0xffff0000u);
+    f[0] = make_float2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+    f[1] = make_float2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+    f[2] = make_float2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+    f[3] = make_float2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
 }
 
 // K/V rows are read exactly once per layer: read-only path, no L1 allocation.
@@ -91,16 +96,106 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f)
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// ---- staged path: bulk copies into shared memory completing on mbarriers
+constexpr int kStageRowBytes = kHeadDim * 2;                   // one bf16 row
+constexpr int kStageBytes = 2 * kTokPerRound * kStageRowBytes;  // K block + V block = 32 KB
+constexpr int kStageTxPerToken = 2 * kStageRowBytes;
+constexpr long kSpinLimit = 1L << 22;  // bounded mbarrier wait (try_wait suspends between polls)
+
+// Ring depth per group size: two CTAs per SM where registers allow it.
+__host__ __device__ constexpr int staged_stages(int G)
+{
+    return G <= 2 ? 3 : (G == 4 ? 2 : 4);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity)
+{
+    const uint32_t addr = smem_u32(bar);
+    for (long i = 0; i < kSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done)
+            return true;
+    }
+    return false;
+}
+
+// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of
+// 16) whose completion is counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, unsigned bytes,
+                                              uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 16-byte global -> shared copy through L2 only (cp.async.cg); completion is
+// tracked per thread in commit groups.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const unsigned char *p)
+{
+    return *reinterpret_cast<const uint4 *>(p);
+}
+
 namespace cg = cooperative_groups;
 
 // CLUSTER: the splits of one (batch row, KV head) form a thread-block
 // cluster (grid x = cluster x = splits) and are merged through distributed
 // shared memory; otherwise through global partials and an arrival ticket.
-template <int G, bool SPARSE, bool SELECT, bool CLUSTER>
+// STAGED: rows reach shared memory by bulk copies (see the file comment).
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
 __global__ void __launch_bounds__(kAttnThreads)
 attention_kernel(const AttnArgs a)
 {
     constexpr int U = kTokPerHalf;
+    constexpr int S = staged_stages(G);
+    extern __shared__ __align__(128) unsigned char sm_stage[];  // STAGED: [S][K rows | V rows]
+    __shared__ __align__(8) uint64_t sm_full[STAGED ? S : 1];
     __shared__ float sm_m[kAttnWarps][G];
     __shared__ float sm_l[kAttnWarps][G];
     __shared__ float sm_w[kAttnWarps][G];
@@ -178,59 +273,139 @@ attention_kernel(const AttnArgs a)
             vr[u] = ok[u] ? load_row16(vbase + (size_t)row * kHeadDim) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
+    // Staged: stage `it` of the ring receives the 64 tokens starting at
+    // t0 + it * 64.  Full layers: bulk copies of the K and V blocks, issued
+    // by warp 0 and completing on the stage's mbarrier.
+    const int n_it = t1 > t0 ? (t1 - t0 + kTokPerRound - 1) / kTokPerRound : 0;
+    const uint16_t *krows = a.k + bg * (size_t)a.Nmax * kHeadDim;
+    const uint16_t *vrows = a.v + bg * (size_t)a.Nmax * kHeadDim;
+    auto issue_stage = [&](int it) {  // full layers, warp 0
+        unsigned char *kst = sm_stage + (it % S) * kStageBytes;
+        unsigned char *vst = kst + kStageBytes / 2;
+        uint64_t *bar = &sm_full[it % S];
+        const int base = t0 + it * kTokPerRound;
+        // contiguous rows: one copy for the K block, one for the V block
+        const int n = min(kTokPerRound, t1 - base);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, (unsigned)n * kStageTxPerToken);
+            bulk_copy_g2s(kst, krows + (size_t)base * kHeadDim, (unsigned)n * kStageRowBytes,
+                          bar);
+            bulk_copy_g2s(vst, vrows + (size_t)base * kHeadDim, (unsigned)n * kStageRowBytes,
+                          bar);
+        }
+    };
+
+    // Sparse layers: each thread copies the 16-byte pieces it will read itself
+    // (lane c of a half-warp: bytes 16c.. of the K and V rows of its U
+    // tokens) with cp.async, one commit group per stage (empty past the end),
+    // so a thread only ever waits for its own copies: no barrier in the loop.
+    auto issue_rows_cp = [&](int it) {
+        if (it < n_it) {
+            unsigned char *kst = sm_stage + (it % S) * kStageBytes;
+            unsigned char *vst = kst + kStageBytes / 2;
+            const int slot0 = (warp * 2 + half) * U;
+            const int tb = t0 + it * kTokPerRound + slot0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = tb + u;
+                const int row = t < t1 ? sm_rows[t - t0] : -1;
+                if (row >= 0) {
+                    cp_async16(kst + (slot0 + u) * kStageRowBytes + c * 16,
+                                krows + (size_t)row * kHeadDim + c * 8);
+                    cp_async16(vst + (slot0 + u) * kStageRowBytes + c * 16,
+                                vrows + (size_t)row * kHeadDim + c * 8);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
     // The cache is never written by a kernel of the step, so the first round
-    // is requested before waiting for the previous kernel; q may come from it.
+    // (register-streamed) or the first S stages (staged) are requested before
+    // waiting for the previous kernel; q may come from it.
     uint4 kr0[U], vr0[U];
     bool ok0[U];
-    load_round(t0, kr0, vr0, ok0);
+    if constexpr (STAGED && SPARSE) {
+        for (int it = 0; it < S; ++it)
+            issue_rows_cp(it);
+    } else if constexpr (STAGED) {
+        if (tid == 0) {
+            for (int i = 0; i < S; ++i)
+                mbar_init(&sm_full[i], 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        if (warp == 0)
+            for (int it = 0; it < S && it < n_it; ++it)
+                issue_stage(it);
+    } else {
+        load_round(t0, kr0, vr0, ok0);
+    }
     pdl_wait();
 
-    // This lane's 8 dims of the group's G queries.
-    float qf[G][8];
+    // This lane's 8 dims of the group's G queries, as 4 dim pairs.
+    float2 q2[G][4];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         const uint4 qv = *reinterpret_cast<const uint4 *>(
             a.q + ((size_t)b * a.Hq + (size_t)g * G + h) * kHeadDim + c * 8);
-        unpack8(qv, qf[h]);
+        unpack8x2(qv, q2[h]);
     }
 
     const float c2 = a.scale * kLog2e;  // logits in log2 units for exp2
-    float m[G], l[G], o[G][8];
+    float m[G], l[G];
+    float2 o[G][4];  // un-normalised output, dim pairs
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         m[h] = -CUDART_INF_F;
         l[h] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            o[h][i] = 0.0f;
+        for (int j = 0; j < 4; ++j)
+            o[h][j] = make_float2(0.0f, 0.0f);
     }
 
     // One round: scores, online softmax and P V for this half-warp's U tokens.
     auto round = [&](int base, const uint4 (&kr)[U], const uint4 (&vr)[U], const bool (&ok)[U]) {
         const int tb = base + (warp * 2 + half) * U;  // this half-warp's first token
 
-        // q . k over this lane's 8 dims, then over the half-warp's 16 lanes.
-        float dot[G][U];
+        // q . k over this lane's 8 dims (even and odd dims in the two
+        // halves of a packed accumulator), then over the half-warp's 16
+        // lanes, two (head, token) sums per packed add.
+        static_assert(U % 2 == 0, "tokens are reduced in pairs");
+        float2 dp[G][U / 2];  // (dot[h][2v], dot[h][2v+1])
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            float kf[8];
-            unpack8(kr[u], kf);
+            float2 k2[4];
+            unpack8x2(kr[u], k2);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float acc = 0.0f;
+                float2 acc = __fmul2_rn(q2[h][0], k2[0]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc = fmaf(qf[h][i], kf[i], acc);
-                dot[h][u] = acc;
+                for (int j = 1; j < 4; ++j)
+                    acc = __ffma2_rn(q2[h][j], k2[j], acc);
+                const float d = acc.x + acc.y;
+                if (u & 1)
+                    dp[h][u / 2].y = d;
+                else
+                    dp[h][u / 2].x = d;
             }
         }
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int u = 0; u < U; ++u)
+            for (int v2 = 0; v2 < U / 2; ++v2)
 #pragma unroll
-                for (int off = 8; off >= 1; off >>= 1)
-                    dot[h][u] += __shfl_xor_sync(kFull, dot[h][u], off);
+                for (int off = 8; off >= 1; off >>= 1) {
+                    const float2 t = make_float2(__shfl_xor_sync(kFull, dp[h][v2].x, off),
+                                                 __shfl_xor_sync(kFull, dp[h][v2].y, off));
+                    dp[h][v2] = __fadd2_rn(dp[h][v2], t);
+                }
+        float dot[G][U];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                dot[h][u] = (u & 1) ? dp[h][u / 2].y : dp[h][u / 2].x;
 
         if constexpr (SELECT) {
             // Selection score of a KV head: the sum of its query heads'
@@ -272,9 +447,10 @@ attention_kernel(const AttnArgs a)
                     ps += p[h][u];
                 }
                 l[h] = l[h] * alpha + ps;
+                const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    o[h][i] *= alpha;
+                for (int j = 0; j < 4; ++j)
+                    o[h][j] = __fmul2_rn(o[h][j], al2);
                 m[h] = m_new;
             } else {
 #pragma unroll
@@ -284,22 +460,89 @@ attention_kernel(const AttnArgs a)
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            float vf[8];
-            unpack8(vr[u], vf);
+            float2 v2[4];
+            unpack8x2(vr[u], v2);
 #pragma unroll
-            for (int h = 0; h < G; ++h)
+            for (int h = 0; h < G; ++h) {
+                const float2 p2 = make_float2(p[h][u], p[h][u]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    o[h][i] = fmaf(p[h][u], vf[i], o[h][i]);
+                for (int j = 0; j < 4; ++j)
+                    o[h][j] = __ffma2_rn(p2, v2[j], o[h][j]);
+            }
         }
     };
-    if (t0 < t1)
-        round(t0, kr0, vr0, ok0);
-    for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
-        uint4 kr[U], vr[U];
-        bool ok[U];
-        load_round(base, kr, vr, ok);
-        round(base, kr, vr, ok);
+    if constexpr (STAGED && SPARSE) {
+        const int slot0 = (warp * 2 + half) * U;
+        for (int it = 0; it < n_it; ++it) {
+            cp_async_wait<S - 1>();  // this thread's copies of stage `it` have landed
+            const unsigned char *kst = sm_stage + (it % S) * kStageBytes;
+            const unsigned char *vst = kst + kStageBytes / 2;
+            const int base = t0 + it * kTokPerRound;
+            uint4 kr[U], vr[U];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = base + slot0 + u;
+                ok[u] = t < t1 && sm_rows[t - t0] >= 0;
+                kr[u] = ok[u] ? lds128(kst + (slot0 + u) * kStageRowBytes + c * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
+                vr[u] = ok[u] ? lds128(vst + (slot0 + u) * kStageRowBytes + c * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
+            }
+            round(base, kr, vr, ok);
+            issue_rows_cp(it + S);  // refill the slot just consumed (its values are used above)
+        }
+        cp_async_wait<0>();
+    } else if constexpr (STAGED) {
+        int it = 0;
+        bool failed = false;
+        for (; it < n_it; ++it) {
+            const int st = it % S;
+            // false only if a copy never completed: reported, the CTA stops below
+            const bool landed = mbar_wait(&sm_full[st], (unsigned)(it / S) & 1u);
+            const unsigned char *kst = sm_stage + st * kStageBytes;
+            const unsigned char *vst = kst + kStageBytes / 2;
+            const int base = t0 + it * kTokPerRound;
+            const int slot0 = (warp * 2 + half) * U;
+            uint4 kr[U], vr[U];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = base + slot0 + u;
+                ok[u] = t < t1 && (!SPARSE || sm_rows[t - t0] >= 0);
+                kr[u] = ok[u] ? lds128(kst + (slot0 + u) * kStageRowBytes + c * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
+                vr[u] = ok[u] ? lds128(vst + (slot0 + u) * kStageRowBytes + c * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
+            }
+            round(base, kr, vr, ok);
+            failed = __syncthreads_or(!landed);  // also: every warp is done with stage st
+            if (failed)
+                break;
+            if (warp == 0 && it + S < n_it) {
+                // the ring slot is free: order the reads above before the async-proxy writes
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_stage(it + S);
+            }
+        }
+        if (failed) {
+            // stages still in flight land before the CTA exits (bounded), then report
+            if (tid == 0) {
+                for (int j = it + 1; j < n_it && j < it + S; ++j)
+                    mbar_wait(&sm_full[j % S], (unsigned)(j / S) & 1u);
+                atomicOr(a.status, kFlagWaitTimeout);
+            }
+            return;
+        }
+    } else {
+        if (t0 < t1)
+            round(t0, kr0, vr0, ok0);
+        for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
+            uint4 kr[U], vr[U];
+            bool ok[U];
+            load_round(base, kr, vr, ok);
+            round(base, kr, vr, ok);
+        }
     }
 
     pdl_launch_dependents();  // the next kernel's CTAs may start requesting their cache rows
@@ -314,9 +557,10 @@ attention_kernel(const AttnArgs a)
         const float so = safe_exp2_diff(m_o, m_new);
         l[h] = l[h] * sa + l_o * so;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float oo = __shfl_xor_sync(kFull, o[h][i], 16);
-            o[h][i] = o[h][i] * sa + oo * so;
+        for (int j = 0; j < 4; ++j) {
+            const float2 oo = make_float2(__shfl_xor_sync(kFull, o[h][j].x, 16),
+                                          __shfl_xor_sync(kFull, o[h][j].y, 16));
+            o[h][j] = make_float2(o[h][j].x * sa + oo.x * so, o[h][j].y * sa + oo.y * so);
         }
         m[h] = m_new;
     }
@@ -328,8 +572,8 @@ attention_kernel(const AttnArgs a)
                 sm_l[warp][h] = l[h];
             }
             float4 *dst = reinterpret_cast<float4 *>(&sm_o[warp][h][c * 8]);
-            dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-            dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+            dst[0] = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+            dst[1] = make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
         }
     }
     __syncthreads();
@@ -503,16 +747,46 @@ attention_kernel(const AttnArgs a)
 
 int g_carveout = -1;  // preferred shared-memory carveout (percent) for the attention kernels
 
-template <int G, bool SPARSE, bool SELECT, bool CLUSTER>
+template <int G, bool STAGED>
+constexpr size_t dyn_smem_bytes()
+{
+    return STAGED ? (size_t)staged_stages(G) * kStageBytes : 0;
+}
+
+// The dynamic shared-memory opt-in of the staged kernels, once per device.
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
+cudaError_t configure_once()
+{
+    if (!STAGED)
+        return cudaSuccess;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64 && configured[dev])
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(attention_kernel<G, SPARSE, SELECT, CLUSTER, STAGED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dyn_smem_bytes<G, STAGED>());
+    if (e == cudaSuccess && dev >= 0 && dev < 64)
+        configured[dev] = true;
+    return e;
+}
+
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
 cudaError_t launch_one(const AttnArgs &a, int batch, cudaStream_t stream)
 {
+    auto kern = attention_kernel<G, SPARSE, SELECT, CLUSTER, STAGED>;
     if (g_carveout >= 0)
-        cudaFuncSetAttribute(attention_kernel<G, SPARSE, SELECT, CLUSTER>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout, g_carveout);
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, g_carveout);
+    cudaError_t e0 = configure_once<G, SPARSE, SELECT, CLUSTER, STAGED>();
+    if (e0 != cudaSuccess)
+        return e0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.nsplit, (unsigned)a.Hkv, (unsigned)batch);
     cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = dyn_smem_bytes<G, STAGED>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -520,8 +794,7 @@ cudaError_t launch_one(const AttnArgs &a, int batch, cudaStream_t stream)
     int nattr = 1;
     if (CLUSTER) {
         if (a.nsplit > 8) {  // beyond the portable cluster size
-            cudaError_t e = cudaFuncSetAttribute(attention_kernel<G, SPARSE, SELECT, CLUSTER>,
-                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess)
                 return e;
         }
@@ -533,15 +806,18 @@ cudaError_t launch_one(const AttnArgs &a, int batch, cudaStream_t stream)
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return cudaLaunchKernelEx(&cfg, attention_kernel<G, SPARSE, SELECT, CLUSTER>, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int G, bool SPARSE, bool SELECT>
+template <int G, bool SPARSE, bool SELECT, bool STAGED>
 int occupancy_one()
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<G, SPARSE, SELECT, false>,
-                                                      kAttnThreads, 0) != cudaSuccess)
+    if (configure_once<G, SPARSE, SELECT, false, STAGED>() != cudaSuccess)
+        return 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, attention_kernel<G, SPARSE, SELECT, false, STAGED>, kAttnThreads,
+            dyn_smem_bytes<G, STAGED>()) != cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
 }
@@ -550,19 +826,23 @@ int occupancy_one()
 
 void set_attention_carveout(int percent) { g_carveout = percent; }
 
-cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, const AttnArgs &a,
-                             int batch, cudaStream_t stream)
+cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, bool staged,
+                             const AttnArgs &a, int batch, cudaStream_t stream)
 {
-#define TD_DISPATCH_G(GG)                                                             \
-    case GG:                                                                          \
-        if (sparse)                                                                   \
-            return cluster ? launch_one<GG, true, false, true>(a, batch, stream)      \
-                           : launch_one<GG, true, false, false>(a, batch, stream);    \
-        if (select)                                                                   \
-            return cluster ? launch_one<GG, false, true, true>(a, batch, stream)      \
-                           : launch_one<GG, false, true, false>(a, batch, stream);    \
-        return cluster ? launch_one<GG, false, false, true>(a, batch, stream)         \
-                       : launch_one<GG, false, false, false>(a, batch, stream);
+    // the cluster merge is built for the register-streamed kernels only
+#define TD_DISPATCH_G(GG)                                                                   \
+    case GG:                                                                                \
+        if (sparse)                                                                         \
+            return cluster   ? launch_one<GG, true, false, true, false>(a, batch, stream)   \
+                   : staged ? launch_one<GG, true, false, false, true>(a, batch, stream)   \
+                            : launch_one<GG, true, false, false, false>(a, batch, stream); \
+        if (select)                                                                         \
+            return cluster   ? launch_one<GG, false, true, true, false>(a, batch, stream)   \
+                   : staged ? launch_one<GG, false, true, false, true>(a, batch, stream)   \
+                            : launch_one<GG, false, true, false, false>(a, batch, stream); \
+        return cluster   ? launch_one<GG, false, false, true, false>(a, batch, stream)      \
+               : staged ? launch_one<GG, false, false, false, true>(a, batch, stream)      \
+                        : launch_one<GG, false, false, false, false>(a, batch, stream);
     switch (G) {
         TD_DISPATCH_G(1)
         TD_DISPATCH_G(2)
@@ -574,15 +854,18 @@ cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, cons
 #undef TD_DISPATCH_G
 }
 
-int attention_ctas_per_sm(int G, bool sparse, bool select)
+int attention_ctas_per_sm(int G, bool sparse, bool select, bool staged)
 {
-#define TD_OCC_G(GG)                                                      \
-    case GG:                                                              \
-        if (sparse)                                                       \
-            return occupancy_one<GG, true, false>();                      \
-        if (select)                                                       \
-            return occupancy_one<GG, false, true>();                      \
-        return occupancy_one<GG, false, false>();
+#define TD_OCC_G(GG)                                                                      \
+    case GG:                                                                              \
+        if (sparse)                                                                       \
+            return staged ? occupancy_one<GG, true, false, true>()                        \
+                          : occupancy_one<GG, true, false, false>();                      \
+        if (select)                                                                       \
+            return staged ? occupancy_one<GG, false, true, true>()                        \
+                          : occupancy_one<GG, false, true, false>();                      \
+        return staged ? occupancy_one<GG, false, false, true>()                           \
+                      : occupancy_one<GG, false, false, false>();
     switch (G) {
         TD_OCC_G(1)
         TD_OCC_G(2)

@@ -20,14 +20,14 @@ constexpr int kPortableClusterSplits = 8;  // the split counts merged through a 
 constexpr int kMaxSplitCtas = 8192;    // cap on batch * kv_heads * splits for partials
 constexpr int kMaxSparseChunk = 2048;  // index entries one sparse CTA stages in shared memory
 constexpr int kMaxTopK = kMaxSplits * kMaxSparseChunk;
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkCandidates = 16384;  // (key, position) pairs a top-k CTA holds in shared memory
+constexpr int kTopkCandidates = 16384;  // (key, position) pairs a 1024-thread top-k CTA holds in shared memory
 constexpr int kSelectBits = 11;         // first radix digit of the top-k select (key bits 31..21)
 constexpr int kSelectBins = 1 << kSelectBits;
 constexpr int kTopkBitmapBits = 1 << 18; // rows up to this length are compacted through a bitmap
 
 constexpr uint32_t kFlagIndexOutOfRange = 0x1u;
 constexpr uint32_t kFlagSeqLenOutOfRange = 0x2u;
+constexpr uint32_t kFlagWaitTimeout = 0x4u;  // a bounded wait for an async copy gave up
 
 // One attention launch (full or sparse).  Partials are struct-of-arrays over
 // (batch*kv_head, split, head-in-group[, dim]) with split stride `nsplit`.
@@ -65,14 +65,18 @@ struct TopkArgs {
 // G = query heads per KV head (1, 2, 4, 8).
 // cluster: merge the splits through a thread-block cluster (requires
 // a.nsplit <= kMaxClusterSplits); otherwise through global partials.
-cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, const AttnArgs &a,
-                             int batch, cudaStream_t stream);
-cudaError_t launch_topk(const TopkArgs &a, int batch, cudaStream_t stream);
+// staged: K/V rows reach shared memory by bulk asynchronous copies into a
+// ring of stages (ignored when cluster is set); otherwise register-streamed.
+cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, bool staged,
+                             const AttnArgs &a, int batch, cudaStream_t stream);
+// threads: 1024 or 512 threads per row's CTA; 0 picks 1024 when the rows fit
+// one wave on the device's SMs, else 512 (two CTAs per SM).
+cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, cudaStream_t stream);
 
 // Preferred shared-memory carveout (percent, -1 = driver default) for later attention launches.
 void set_attention_carveout(int percent);
 
 // Resident CTAs per SM of one attention instantiation (occupancy query).
-int attention_ctas_per_sm(int G, bool sparse, bool select);
+int attention_ctas_per_sm(int G, bool sparse, bool select, bool staged);
 
 }  // namespace td

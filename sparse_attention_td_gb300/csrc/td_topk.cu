@@ -8,8 +8,8 @@
 // Ties at the k-th score go to the lower position; the result is written in
 // ascending position order and padded with -1 when seq_lens[b] < k.
 //
-// Method: exact radix select on order-preserving 32-bit keys, one 1024-thread
-// CTA per row:
+// Method: exact radix select on order-preserving 32-bit keys, one CTA (1024
+// or 512 threads) per row:
 //   1. an 11-bit histogram of the keys' top bits picks the bin holding the
 //      k-th largest key.  In a selection layer the attention kernel that
 //      wrote the scores already built it (and this kernel clears it again);
@@ -35,15 +35,12 @@ namespace td {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kT = kTopkThreads;        // 1024
-constexpr int kWarps = kT / 32;         // 32
 constexpr int kBatch = 16;              // loads in flight per thread
 constexpr int kBatchV = 4;              // float4 loads in flight per thread (16 scores)
 constexpr unsigned kWarpSelectMax = 2048; // threshold bins up to this size finish in one warp
 constexpr int kBits1 = kSelectBits;     // first digit: key bits 31..21
 constexpr int kBins1 = kSelectBins;     // 2048
 constexpr int kBitmapWords = kTopkBitmapBits / 32;
-constexpr int kWordsPerThread = kBitmapWords / kT;
 constexpr int kSubHists = 4;            // pass-1 sub-histograms (less atomic contention)
 
 // Programmatic dependent launch (see td_attn.cu): the scores come from the
@@ -69,9 +66,23 @@ __device__ __forceinline__ uint32_t order_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The kernel is instantiated for two block sizes: 1024 threads (one CTA per
+// SM, for launches with fewer rows than SMs) and 512 threads (two CTAs per SM
+// in 64 registers a thread, so many rows run in a single wave).
+template <int NT>
+struct TopkCfg {
+    static constexpr int kT = NT;
+    static constexpr int kWarps = NT / 32;
+    static constexpr int kWordsPerThread = kBitmapWords / NT;
+    static constexpr int kCand = NT >= 1024 ? kTopkCandidates : kTopkCandidates / 2;  // (key, pos) pairs
+    static constexpr int kMinBlocks = 1024 / NT;
+};
+
+template <int NT>
 struct TopkSmem {
-    unsigned hist[kSubHists * kBins1];  // 32 KB; pass-1 sub-histograms, later one 256-bin histogram
-    unsigned scan[kWarps];
+    static constexpr int kWarps = NT / 32;
+    unsigned hist[kBins1];              // first-digit histogram, later a 256-bin scratch histogram
+    unsigned scan[32];                  // per-warp partial sums (entries >= kWarps stay unused)
     unsigned tot[kBatch * kWarps];
     unsigned pre[kBatch * kWarps];
     unsigned res[2];                    // digit, remaining rank
@@ -82,9 +93,10 @@ struct TopkSmem {
 // Block-wide search over a histogram of NB bins (digit = bin index): the
 // digit d with count(> d) < r <= count(>= d).  Writes d and r - count(> d)
 // to sm.res.  All threads must call it.
-template <int NB>
-__device__ void find_digit(TopkSmem &sm, const unsigned *hist, unsigned r)
+template <int NB, int NT>
+__device__ void find_digit(TopkSmem<NT> &sm, const unsigned *hist, unsigned r)
 {
+    constexpr int kT = NT, kWarps = NT / 32;
     constexpr int per = NB >= kT ? NB / kT : 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int first = NB - 1 - tid * per;  // this thread's highest bin
@@ -102,7 +114,7 @@ __device__ void find_digit(TopkSmem &sm, const unsigned *hist, unsigned r)
         sm.scan[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        unsigned w = sm.scan[lane], wi = w;
+        unsigned w = lane < kWarps ? sm.scan[lane] : 0u, wi = w;
         for (int off = 1; off < 32; off <<= 1) {
             const unsigned v = __shfl_up_sync(kFull, wi, off);
             if (lane >= off)
@@ -129,8 +141,10 @@ __device__ void find_digit(TopkSmem &sm, const unsigned *hist, unsigned r)
 }
 
 // Exclusive prefix sum of v over the block (thread order); *total gets the sum.
-__device__ __forceinline__ unsigned block_exclusive_sum(TopkSmem &sm, unsigned v, unsigned *total)
+template <int NT>
+__device__ __forceinline__ unsigned block_exclusive_sum(TopkSmem<NT> &sm, unsigned v, unsigned *total)
 {
+    constexpr int kWarps = NT / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     unsigned incl = v;
     for (int off = 1; off < 32; off <<= 1) {
@@ -142,7 +156,7 @@ __device__ __forceinline__ unsigned block_exclusive_sum(TopkSmem &sm, unsigned v
         sm.scan[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const unsigned w = sm.scan[lane];
+        const unsigned w = lane < kWarps ? sm.scan[lane] : 0u;
         unsigned wi = w;
         for (int off = 1; off < 32; off <<= 1) {
             const unsigned t = __shfl_up_sync(kFull, wi, off);
@@ -160,10 +174,11 @@ __device__ __forceinline__ unsigned block_exclusive_sum(TopkSmem &sm, unsigned v
     return excl;
 }
 
-// Calls f(key, pos) for every position of the row, eight loads in flight per thread.
-template <class F>
+// Calls f(key, pos) for every position of the row, kBatch loads in flight per thread.
+template <int NT, class F>
 __device__ __forceinline__ void stream_row(const float *s, int n, F f)
 {
+    constexpr int kT = NT;
     for (int base = 0; base < n; base += kT * kBatch) {
         float v[kBatch];
 #pragma unroll
@@ -186,8 +201,8 @@ __device__ __forceinline__ void stream_row(const float *s, int n, F f)
 // for every pair.  Returns the value; *rank_out receives r minus the count of
 // larger values (how many items equal to the result belong in the set) and
 // *eq_out the number of items equal to it.
-template <class Src>
-__device__ uint32_t radix_select(TopkSmem &sm, Src src, int hi_bit, uint32_t prefix,
+template <int NT, class Src>
+__device__ uint32_t radix_select(TopkSmem<NT> &sm, Src src, int hi_bit, uint32_t prefix,
                                  uint32_t mask, unsigned r, unsigned *rank_out, unsigned *eq_out)
 {
     unsigned *hist = sm.hist;
@@ -196,7 +211,7 @@ __device__ uint32_t radix_select(TopkSmem &sm, Src src, int hi_bit, uint32_t pre
         const int width = top + 1 < 8 ? top + 1 : 8;
         const int shift = top + 1 - width;
         const unsigned dmask = (1u << width) - 1u;
-        for (int i = threadIdx.x; i < 256; i += kT)
+        for (int i = threadIdx.x; i < 256; i += NT)
             hist[i] = 0u;
         __syncthreads();
         src([&](uint32_t val, int) {
@@ -285,13 +300,16 @@ __device__ uint32_t warp_select(unsigned *hist, unsigned n, ValF val, KeepF keep
     return prefix;
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 1)
+template <int NT>
+__global__ void __launch_bounds__(NT, TopkCfg<NT>::kMinBlocks)
 topk_kernel(const TopkArgs a)
 {
+    using C = TopkCfg<NT>;
+    constexpr int kT = C::kT, kWarps = C::kWarps, kWordsPerThread = C::kWordsPerThread;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    TopkSmem &sm = *reinterpret_cast<TopkSmem *>(smem_raw);
-    uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem_raw + sizeof(TopkSmem));
-    int32_t *cand_pos = reinterpret_cast<int32_t *>(cand_key + kTopkCandidates);
+    TopkSmem<NT> &sm = *reinterpret_cast<TopkSmem<NT> *>(smem_raw);
+    uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem_raw + sizeof(TopkSmem<NT>));
+    int32_t *cand_pos = reinterpret_cast<int32_t *>(cand_key + C::kCand);
 
     const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -328,16 +346,18 @@ topk_kernel(const TopkArgs a)
             ghist[i] = 0u;
         }
     } else {
+        // sub-histograms (less atomic contention) in the candidate area, unused until pass 2
+        unsigned *sub = reinterpret_cast<unsigned *>(cand_key);
         for (int i = tid; i < kSubHists * kBins1; i += kT)
-            sm.hist[i] = 0u;
+            sub[i] = 0u;
         __syncthreads();
-        unsigned *mine = sm.hist + (warp % kSubHists) * kBins1;
-        stream_row(s, n, [&](uint32_t key, int) { atomicAdd(&mine[key >> (32 - kBits1)], 1u); });
+        unsigned *mine = sub + (warp % kSubHists) * kBins1;
+        stream_row<NT>(s, n, [&](uint32_t key, int) { atomicAdd(&mine[key >> (32 - kBits1)], 1u); });
         __syncthreads();
         for (int i = tid; i < kBins1; i += kT) {
             unsigned t = 0;
             for (int h = 0; h < kSubHists; ++h)
-                t += sm.hist[h * kBins1 + i];
+                t += sub[h * kBins1 + i];
             sm.hist[i] = t;
         }
     }
@@ -354,7 +374,7 @@ topk_kernel(const TopkArgs a)
     unsigned need_eq, n_eq;
     int P = 0x7fffffff;  // largest kept position among keys == T
     const bool use_bitmap = n <= kTopkBitmapBits;
-    if (bin_count <= (unsigned)kTopkCandidates) {
+    if (bin_count <= (unsigned)C::kCand) {
         // 2. gather the threshold bin into shared memory, finish there; rows
         //    that fit the bitmap also mark every key above the bin as selected
         if (use_bitmap) {
@@ -531,11 +551,11 @@ topk_kernel(const TopkArgs a)
         }
     } else {
         // threshold bin too large for shared memory: stream the remaining digits
-        auto row_src = [&](auto f) { stream_row(s, n, f); };
+        auto row_src = [&](auto f) { stream_row<NT>(s, n, f); };
         T = radix_select(sm, row_src, 31 - kBits1, prefix1, mask1, r1, &need_eq, &n_eq);
         if (need_eq < n_eq) {
             auto eq_src = [&](auto f) {
-                stream_row(s, n, [&](uint32_t key, int i) {
+                stream_row<NT>(s, n, [&](uint32_t key, int i) {
                     if (key == T)
                         f(~(uint32_t)i, 0);
                 });
@@ -605,23 +625,26 @@ topk_kernel(const TopkArgs a)
     }
 }
 
-}  // namespace
-
-size_t topk_smem_bytes()
+template <int NT>
+constexpr size_t topk_smem_bytes()
 {
-    return sizeof(TopkSmem) + (size_t)kTopkCandidates * (sizeof(uint32_t) + sizeof(int32_t));
+    return sizeof(TopkSmem<NT>) + (size_t)TopkCfg<NT>::kCand * (sizeof(uint32_t) + sizeof(int32_t));
 }
 
-cudaError_t launch_topk(const TopkArgs &a, int batch, cudaStream_t stream)
+static_assert(kSubHists * kBins1 <= 2 * TopkCfg<512>::kCand, "pass-1 sub-histograms fit in the candidate area");
+static_assert(2 * (topk_smem_bytes<512>() + 1024) <= 228 * 1024, "two 512-thread CTAs fit one SM");
+
+template <int NT>
+cudaError_t launch_topk_nt(const TopkArgs &a, int batch, cudaStream_t stream)
 {
-    const size_t smem = topk_smem_bytes();
+    constexpr size_t smem = topk_smem_bytes<NT>();
     static bool configured[64] = {false};  // the smem opt-in is per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess)
             return e;
@@ -630,7 +653,7 @@ cudaError_t launch_topk(const TopkArgs &a, int batch, cudaStream_t stream)
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)batch);
-    cfg.blockDim = dim3(kTopkThreads);
+    cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -638,7 +661,24 @@ cudaError_t launch_topk(const TopkArgs &a, int batch, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_kernel, a);
+    return cudaLaunchKernelEx(&cfg, topk_kernel<NT>, a);
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, cudaStream_t stream)
+{
+    if (threads == 0) {  // one wave of 1024-thread CTAs if the rows fit, else 512-thread pairs
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        threads = (long)a.Hkv * batch > sms ? 512 : 1024;
+    }
+    return threads == 512 ? launch_topk_nt<512>(a, batch, stream)
+                          : launch_topk_nt<1024>(a, batch, stream);
 }
 
 }  // namespace td

@@ -124,5 +124,7 @@ def test_step_schedule_checks(L):
 def test_tuning_keys(L):
     td.td_set_tuning("full_waves", 3)
     td.td_set_tuning("full_waves", 0)     # default again
+    td.td_set_tuning("topk_threads", 512)
+    td.td_set_tuning("topk_threads", 0)
     with pytest.raises(td.TdError):
         td.td_set_tuning("no_such_knob", 1)

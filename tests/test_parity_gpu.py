@@ -26,9 +26,28 @@ def _built():
     td.td_set_tuning("max_splits", 0)
 
 
+@pytest.fixture(scope="module", autouse=True, params=[0, 1], ids=["streamed", "staged"])
+def staged(request):
+    """Every case runs on both ways K/V rows reach the attention kernels:
+    register-streamed loads and bulk copies into shared-memory stages."""
+    td.td_set_tuning("full_staged", request.param)  # both paths for every G
+    td.td_set_tuning("sparse_staged", request.param)
+    yield request.param
+    td.td_set_tuning("full_staged", -1)
+    td.td_set_tuning("sparse_staged", -1)
+
+
 @pytest.fixture(scope="module")
 def orc():
     return oracle.get()
+
+
+@pytest.fixture(params=[1024, 512])
+def topk_threads(request):
+    """Both block sizes of the top-k kernel (the default picks by row count)."""
+    td.td_set_tuning("topk_threads", request.param)
+    yield request.param
+    td.td_set_tuning("topk_threads", 0)
 
 
 def _dev(*ts):
@@ -89,7 +108,7 @@ def test_full_attention_planted_large_logits(orc):
 
 
 @pytest.mark.parametrize("G,k", [(1, 64), (4, 100), (8, 256), (2, 1)])
-def test_full_select_scores_and_sets(orc, G, k):
+def test_full_select_scores_and_sets(orc, G, k, topk_threads):
     Hkv, B, N = 2, 3, 1500
     lens = [1500, 777, 50]              # the last row has fewer tokens than k for k >= 64
     shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
@@ -126,7 +145,7 @@ def _topk_case(scores_rows, lens, k):
     return arr, idx.cpu().numpy()
 
 
-def test_topk_adversarial(orc):
+def test_topk_adversarial(orc, topk_threads):
     rs = np.random.RandomState(5)
     N = 5000
     rows = [
@@ -149,7 +168,7 @@ def test_topk_adversarial(orc):
             assert np.array_equal(got[b, 0], want), f"row {b} k={k}"
 
 
-def test_topk_large_rows(orc):
+def test_topk_large_rows(orc, topk_threads):
     rs = np.random.RandomState(6)
     N, k = 102400, 4096
     rows = [np.round(rs.randn(N) * 50).astype(np.float32) for _ in range(3)]
@@ -160,9 +179,10 @@ def test_topk_large_rows(orc):
         assert np.array_equal(got[b, 0], want), f"row {b}"
 
 
-def test_topk_threshold_bin_larger_than_shared_memory(orc):
-    """More than 16384 scores share the threshold's top bits: the kernel's
-    streaming fallback path (heavy ties at and around the k-th score)."""
+def test_topk_threshold_bin_larger_than_shared_memory(orc, topk_threads):
+    """More than 16384 (512-thread CTAs: 8192) scores share the threshold's
+    top bits: the kernel's streaming fallback path (heavy ties at and around
+    the k-th score)."""
     rs = np.random.RandomState(7)
     N = 60000
     rows = [np.zeros(N, np.float32),                                   # one bin, all tied
