@@ -223,6 +223,29 @@ def measured_traffic(workload: str, kernel: str):
     return entry.get("dram_bytes_per_launch")
 
 
+def consecutive_overlap(td, torch, wl, shape, q, K, V, seq, ws, device):
+    """Mean fraction of layer l's top-k set that layer l+1 also selects
+    (layers 2..L-1, every (batch row, KV head)), from td_full_attn_select sets
+    and td_index_overlap counts."""
+    if wl.layers < 4:
+        return None
+    sets = []
+    out = torch.empty_like(q[0])
+    for layer in range(2, wl.layers):
+        s = torch.full((wl.batch, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device=device)
+        td.td_full_attn_select(shape, q[layer], K[layer], V[layer], seq, wl.top_k, s, out, None,
+                               None, ws)
+        sets.append(s)
+    counts = torch.empty((wl.batch, wl.kv_heads), dtype=torch.int32, device=device)
+    size = torch.clamp(seq.to(torch.float32), max=float(wl.top_k)).view(-1, 1)
+    rates = []
+    for a, b in zip(sets[:-1], sets[1:]):
+        td.td_index_overlap(shape, a, b, wl.top_k, counts)
+        rates.append((counts.to(torch.float32) / size).mean().item())
+    return {"mean": round(float(np.mean(rates)), 4), "min": round(float(np.min(rates)), 4),
+            "layers": f"2..{wl.layers - 1}"}
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args, world, rank, local):
     import torch
@@ -251,8 +274,10 @@ def run_ours(args, world, rank, local):
     ws = td.Workspace(shape, wl.top_k, device=device)
     modes = list(wl.modes)
     full_modes = list(W.all_full_schedule(wl.layers))
+    sel_modes = list(W.per_layer_select_schedule(wl.layers))
     plan = td.Plan(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
     plan_full = td.Plan(shape, full_modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
+    plan_sel = td.Plan(shape, sel_modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     K_steps, W_steps = args.steps, args.warmup
@@ -276,6 +301,8 @@ def run_ours(args, world, rank, local):
         plan.launch(stream)
         flush_l2()
         plan_full.launch(stream)
+        flush_l2()
+        plan_sel.launch(stream)
         td.td_decode_step(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws,
                           stream=stream)
     torch.cuda.synchronize(device)
@@ -292,6 +319,9 @@ def run_ours(args, world, rank, local):
         ev_full = graph_pass(plan_full, K_steps)
         torch.cuda.synchronize(device)
         dist_barrier(world, device)
+        ev_sel = graph_pass(plan_sel, K_steps)
+        torch.cuda.synchronize(device)
+        dist_barrier(world, device)
         # pass 2: per-layer events around each layer's launches
         traced = []
         for _ in range(K_steps):
@@ -304,6 +334,7 @@ def run_ours(args, world, rank, local):
         dist_barrier(world, device)
     ppsa_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_ppsa) * 1e3
     full_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_full) * 1e3
+    sel_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_sel) * 1e3
     per_layer = np.array([[e[i].elapsed_time(e[i + 1]) * 1e3 for i in range(wl.layers)]
                           for e in traced])                      # [K, L] us
     traced_step_us = float(np.mean([e[0].elapsed_time(e[-1]) * 1e3 for e in traced]))
@@ -315,6 +346,11 @@ def run_ours(args, world, rank, local):
             by_mode[name] = float(np.mean(layer_mean[sel]))
     ppsa_us = dist_max(ppsa_us, world, device)
     full_us = dist_max(full_us, world, device)
+    sel_us = dist_max(sel_us, world, device)
+
+    # Figure 4(a)'s measure on this data (untimed): the top-k set each layer
+    # would select, and its overlap with the next layer's
+    overlap = consecutive_overlap(td, torch, wl, shape, q, K, V, seq, ws, device)
 
     # e2e: host q in (pinned), graph step, host outputs back, per step
     q_host = [x.cpu().pin_memory() for x in q]
@@ -411,6 +447,9 @@ def run_ours(args, world, rank, local):
             "all_full_kv_gbs": round(bytes_model["kv"]["full"] * wl.layers / (full_us * 1e-6) / 1e9,
                                      1),
             "speedup_vs_all_full": round(full_us / ppsa_us, 3),
+            "per_layer_select_us": round(sel_us, 2),
+            "speedup_vs_per_layer_select": round(sel_us / ppsa_us, 3),
+            "consecutive_layer_overlap": overlap,
             "traced_step_us": round(traced_step_us, 2),
             "layer_us": {k: round(v, 2) for k, v in by_mode.items()},
             "sparse_layer_gbs": round(sparse_gbs, 1) if sparse_gbs else None,

@@ -134,6 +134,26 @@ td_status td_topk_select(const td_shape *shape, const float *scores, const int32
                          void *stream);
 
 /*
+ * Overlap of two index sets, per (batch row, KV head): counts[b][g] =
+ * |A[b][g] ∩ B[b][g]|, the number of positions present in both.  This is the
+ * measure behind the review's token-selection sensitivity analysis (§三
+ * "Token selection layer sensitivity", Figure 4(a): the overlap of the most
+ * attended tokens between consecutive layers); the overlap rate is
+ * counts / |A|, with |A| the number of entries >= 0 (min(top_k, N_b) for a
+ * set the library wrote).
+ *   idx_a, idx_b: device int32 [B][Hkv][top_k], each row ascending with -1
+ *     padding only at its end (the layout td_full_attn_select writes);
+ *     entries are positions, compared by value.
+ *   counts: device int32 [B][Hkv] (written, caller-owned).
+ *   top_k >= 1.  Shape as for the other calls (seq_lens are not needed).
+ * Asynchronous on `stream`.  Errors: TD_ERR_INVALID_ARG for null or
+ * misaligned pointers or top_k < 1; TD_ERR_CUDA if the launch fails.  A row
+ * that is not ascending gives an unspecified count (no fault).
+ */
+td_status td_index_overlap(const td_shape *shape, const int32_t *idx_a, const int32_t *idx_b,
+                           int32_t top_k, int32_t *counts, void *stream);
+
+/*
  * One PPSA layer (review §三 "Position Persistent Sparse Attention"):
  *   attention of every query head over the positions idx[b,g(h),0..top_k)
  *   only (entries of -1 are padding and are skipped), with the softmax

@@ -111,6 +111,8 @@ class Oracle:
         L.oracle_decode_step.argtypes = [ctypes.c_int] * 5 + [i32p, ctypes.c_int, i32p,
                                                               ctypes.c_int, ctypes.c_double,
                                                               vpp, vpp, vpp, vpp, i32p]
+        L.oracle_index_overlap.restype = ctypes.c_int
+        L.oracle_index_overlap.argtypes = [i32p, i32p, ctypes.c_int]
         L.oracle_mutant_id.restype = ctypes.c_int
         L.oracle_num_threads.restype = ctypes.c_int
 
@@ -223,6 +225,14 @@ class Oracle:
                                           arr(qs), arr(Ks), arr(Vs), arr(outs),
                                           _ptr(idx, ctypes.c_int32))
         return outs, idx[:, :, :k], rc
+
+    def index_overlap(self, a, b) -> int:
+        """Positions present in both sets (entries < 0 ignored)."""
+        a = np.ascontiguousarray(a, dtype=np.int32)
+        b = np.ascontiguousarray(b, dtype=np.int32)
+        assert a.shape == b.shape and a.ndim == 1
+        return int(self._lib.oracle_index_overlap(_ptr(a, ctypes.c_int32), _ptr(b, ctypes.c_int32),
+                                               len(a)))
 
     def mutant_id(self) -> int:
         return self._lib.oracle_mutant_id()

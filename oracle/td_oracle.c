@@ -20,7 +20,9 @@
  *     token set of the previous selection layer"; Figure 2 rows "PPSA (reuse
  *     selected tokens)");
  *   - the per-step layer schedule [full | full+select | sparse]
- *     (review §三 Figure 2).
+ *     (review §三 Figure 2);
+ *   - the overlap of two token sets (review §三, token-selection
+ *     sensitivity, Figure 4(a)).
  *
  * Readings where the page is silent (each also listed in the design notes):
  *   - "attention score" for selection is the scaled pre-softmax logit a;
@@ -404,6 +406,31 @@ int oracle_decode_step(int B, int Hq, int Hkv, int d, int Nmax, const int32_t *s
         }
     }
     return rc_all;
+}
+
+/*
+ * Overlap of two token sets (review §三 "Token selection layer sensitivity",
+ * Figure 4(a): how many of the most attended tokens two layers share):
+ * the number of positions that occur in both a[0..k) and b[0..k), entries
+ * < 0 (padding) ignored.  Every pair is compared: no order is assumed.
+ */
+int oracle_index_overlap(const int32_t *a, const int32_t *b, int k)
+{
+    int count = 0;
+    for (int i = 0; i < k; ++i) {
+#if ORACLE_MUTANT == 13
+        /* mutant: padding entries are not skipped (a -1 matches a -1) */
+#else
+        if (a[i] < 0)
+            continue;
+#endif
+        for (int j = 0; j < k; ++j)
+            if (b[j] == a[i]) {
+                ++count;
+                break;
+            }
+    }
+    return count;
 }
 
 /* Which mutant this build carries (0 = the oracle itself). */

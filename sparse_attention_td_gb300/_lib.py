@@ -75,6 +75,8 @@ def lib():
     L.td_full_attn_select.argtypes = [shp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
     L.td_topk_select.restype = ctypes.c_int
     L.td_topk_select.argtypes = [shp, vp, vp, i32, vp, vp, sz, vp]
+    L.td_index_overlap.restype = ctypes.c_int
+    L.td_index_overlap.argtypes = [shp, vp, vp, i32, vp, vp]
     L.td_sparse_attn.restype = ctypes.c_int
     L.td_sparse_attn.argtypes = [shp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
     L.td_sparse_attn_noalloc.restype = ctypes.c_int
@@ -205,6 +207,15 @@ def td_topk_select(shape: Shape, scores, seq_lens, top_k, idx_out, ws: Workspace
         _dev(idx_out, "idx_out", torch.int32, nb * shape.num_kv_heads * top_k),
         ws.ptr, ws.nbytes, _stream(stream))
     _check(st, "td_topk_select")
+
+
+def td_index_overlap(shape: Shape, idx_a, idx_b, top_k, counts, stream=None):
+    n = shape.batch * shape.num_kv_heads
+    st = lib().td_index_overlap(
+        ctypes.byref(shape), _dev(idx_a, "idx_a", torch.int32, n * top_k),
+        _dev(idx_b, "idx_b", torch.int32, n * top_k), int(top_k),
+        _dev(counts, "counts", torch.int32, n), _stream(stream))
+    _check(st, "td_index_overlap")
 
 
 def td_sparse_attn(shape: Shape, q, k_cache, v_cache, seq_lens, idx, top_k, out, out_f32=None,

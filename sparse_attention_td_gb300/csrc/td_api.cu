@@ -485,6 +485,22 @@ td_status td_topk_select(const td_shape *shape, const float *scores, const int32
     return TD_OK;
 }
 
+td_status td_index_overlap(const td_shape *shape, const int32_t *idx_a, const int32_t *idx_b,
+                           int32_t top_k, int32_t *counts, void *stream)
+{
+    td_status st = check_shape(shape);
+    if (st)
+        return st;
+    if (top_k < 1 || top_k > td::kMaxTopK || !idx_a || !aligned(idx_a, 4) || !idx_b ||
+        !aligned(idx_b, 4) || !counts || !aligned(counts, 4))
+        return TD_ERR_INVALID_ARG;
+    const int rows = shape->batch * shape->num_kv_heads;
+    if (td::launch_index_overlap(idx_a, idx_b, rows, top_k, counts, (cudaStream_t)stream) !=
+        cudaSuccess)
+        return TD_ERR_CUDA;
+    return TD_OK;
+}
+
 td_status td_sparse_attn(const td_shape *shape, const void *q, const void *k_cache,
                          const void *v_cache, const int32_t *seq_lens, const int32_t *idx,
                          int32_t top_k, void *out, float *out_f32, void *ws, size_t ws_bytes,

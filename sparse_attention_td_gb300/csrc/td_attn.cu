@@ -189,7 +189,8 @@ namespace cg = cooperative_groups;
 // shared memory; otherwise through global partials and an arrival ticket.
 // STAGED: rows reach shared memory by bulk copies (see the file comment).
 template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
-__global__ void __launch_bounds__(kAttnThreads)
+// Register budgets: 64 (MHA, 4 CTAs per SM), 128 (G = 2, 4: 2 CTAs per SM), 255 (G = 8).
+__global__ void __launch_bounds__(kAttnThreads, G == 1 ? 4 : (G <= 4 ? 2 : 1))
 attention_kernel(const AttnArgs a)
 {
     constexpr int U = kTokPerHalf;
@@ -244,8 +245,9 @@ attention_kernel(const AttnArgs a)
         // right before this one produced it: then wait for that kernel first.
         if (a.idx_dep)
             pdl_wait();
-        // Stage this split's persisted positions; -1 is padding, anything
-        // else outside [0, n_b) is reported and skipped.
+        // Stage this split's persisted positions once (every round reads
+        // them from shared memory); -1 is padding, anything else outside
+        // [0, n_b) is reported and skipped.
         const int32_t *ip = a.idx + bg * (size_t)a.top_k;
         for (int j = tid; j < t1 - t0; j += kAttnThreads) {
             int r = ip[t0 + j];
@@ -686,16 +688,22 @@ attention_kernel(const AttnArgs a)
         a.part_m[pbase + tid] = sm_M[tid];
         a.part_l[pbase + tid] = sm_L[tid];
     }
-    __threadfence();
+    // One thread takes the ticket with a release-acquire atomic at GPU scope:
+    // the barrier orders the CTA's partial stores before it, and in the last
+    // CTA the acquire plus the next barrier order the merge's loads after
+    // every other split's release.  No thread-wide fences.
     __syncthreads();
     if (tid == 0) {
-        const unsigned ticket = atomicAdd(&a.tickets[bg], 1u);
+        unsigned ticket;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                     : "=r"(ticket)
+                     : "l"(a.tickets + bg)
+                     : "memory");
         sm_last = (ticket == (unsigned)(nsplit_b - 1));
     }
     __syncthreads();
     if (!sm_last)
         return;
-    __threadfence();
 
     // Last CTA of this (batch, KV head): merge all splits.  Each output
     // element's thread reads every split's (m, l) of its head and its own o

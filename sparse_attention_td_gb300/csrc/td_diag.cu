@@ -1,0 +1,70 @@
+// td_diag.cu -- diagnostics over the persisted index sets.
+//
+// Overlap of two top-k sets per (batch row, KV head): the quantity the
+// TidalDecode review's token-selection sensitivity analysis plots (§三,
+// Figure 4(a): the most attended tokens of consecutive layers overlap
+// heavily, which is what lets a set chosen in one layer serve the next).
+// Both rows are ascending with -1 padding at the end; read with -1 as +inf
+// they stay sorted, so each entry of A is looked up in B by binary search.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "td_internal.h"
+
+namespace td {
+namespace {
+
+constexpr int kOverlapThreads = 256;
+
+__device__ __forceinline__ uint32_t sort_key(int32_t x)
+{
+    return x < 0 ? 0xffffffffu : (uint32_t)x;  // padding sorts last
+}
+
+__global__ void __launch_bounds__(kOverlapThreads)
+overlap_kernel(const int32_t *a, const int32_t *b, int top_k, int32_t *counts)
+{
+    __shared__ unsigned sm_count;
+    const size_t row = blockIdx.x;
+    const int32_t *ra = a + row * (size_t)top_k;
+    const int32_t *rb = b + row * (size_t)top_k;
+    if (threadIdx.x == 0)
+        sm_count = 0u;
+    __syncthreads();
+    unsigned mine = 0;
+    for (int j = threadIdx.x; j < top_k; j += kOverlapThreads) {
+        const int32_t x = __ldg(ra + j);
+        if (x < 0)
+            continue;
+        // first position in rb whose key is >= x
+        int lo = 0, hi = top_k;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sort_key(__ldg(rb + mid)) < (uint32_t)x)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        mine += (lo < top_k && __ldg(rb + lo) == x) ? 1u : 0u;
+    }
+    for (int off = 16; off >= 1; off >>= 1)
+        mine += __shfl_xor_sync(0xffffffffu, mine, off);
+    if ((threadIdx.x & 31) == 0 && mine)
+        atomicAdd(&sm_count, mine);
+    __syncthreads();
+    if (threadIdx.x == 0)
+        counts[row] = (int32_t)sm_count;
+}
+
+}  // namespace
+
+cudaError_t launch_index_overlap(const int32_t *a, const int32_t *b, int rows, int top_k,
+                                 int32_t *counts, cudaStream_t stream)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    overlap_kernel<<<rows, kOverlapThreads, 0, stream>>>(a, b, top_k, counts);
+    return cudaGetLastError();
+}
+
+}  // namespace td

@@ -73,6 +73,10 @@ cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, bool
 // one wave on the device's SMs, else 512 (two CTAs per SM).
 cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, cudaStream_t stream);
 
+// counts[b*Hkv + g] = |a[b][g] ∩ b[b][g]| over two ascending, -1-padded index rows.
+cudaError_t launch_index_overlap(const int32_t *a, const int32_t *b, int rows, int top_k,
+                                 int32_t *counts, cudaStream_t stream);
+
 // Preferred shared-memory carveout (percent, -1 = driver default) for later attention launches.
 void set_attention_carveout(int percent);
 

@@ -367,4 +367,40 @@ def pin_batched_step_equals_groups(orc):
     assert np.all(idx[1] < lens[1])
 
 
+def pin_index_overlap(orc):
+    """Set intersection sizes: identity, disjoint sets, symmetry, padding,
+    and random sets against Python's own set intersection."""
+    a = np.array([3, 9, 12, 40, -1, -1], np.int32)
+    assert orc.index_overlap(a, a) == 4                        # padding is no position
+    assert orc.index_overlap(a, np.array([0, 1, 2, 4, 5, 6], np.int32)) == 0
+    assert orc.index_overlap(np.full(5, -1, np.int32), np.full(5, -1, np.int32)) == 0
+    assert orc.index_overlap(a, np.array([40, 3, -1, -1, -1, -1], np.int32)) == 2  # any order
+    rs = np.random.RandomState(11)
+    for k in (1, 7, 64, 300):
+        for _ in range(5):
+            n = rs.randint(k, 4 * k + 1)
+            x = np.sort(rs.choice(n, k, replace=False)).astype(np.int32)
+            y = np.sort(rs.choice(n, k, replace=False)).astype(np.int32)
+            y[rs.randint(0, k + 1):] = -1                       # a shorter set
+            want = len(set(x.tolist()) & set(int(v) for v in y if v >= 0))
+            assert orc.index_overlap(x, y) == want
+            assert orc.index_overlap(y, x) == want
+
+
+def pin_overlap_of_planted_selections(orc):
+    """Two selection layers whose scores plant sets sharing m positions select
+    sets that overlap in exactly m positions (the Figure 4(a) measure)."""
+    rs = np.random.RandomState(12)
+    n, k, m = 500, 40, 25
+    heavy1 = rs.choice(n, k, replace=False)
+    keep = heavy1[:m]
+    rest = np.setdiff1d(np.arange(n), heavy1)
+    heavy2 = np.concatenate([keep, rs.choice(rest, k - m, replace=False)])
+    s1 = rs.rand(n)
+    s2 = rs.rand(n)
+    s1[heavy1] += 10.0
+    s2[heavy2] += 10.0
+    assert orc.index_overlap(orc.topk(s1, k), orc.topk(s2, k)) == m
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -128,3 +128,14 @@ def test_tuning_keys(L):
     td.td_set_tuning("topk_threads", 0)
     with pytest.raises(td.TdError):
         td.td_set_tuning("no_such_knob", 1)
+
+
+def test_index_overlap_rejects_bad_arguments(L):
+    s = shape()
+    p = ctypes.c_void_p(256)     # never dereferenced: validation fails first
+    assert L.td_index_overlap(ctypes.byref(s), None, p, 8, p, None) == INVALID
+    assert L.td_index_overlap(ctypes.byref(s), p, None, 8, p, None) == INVALID
+    assert L.td_index_overlap(ctypes.byref(s), p, p, 8, None, None) == INVALID
+    assert L.td_index_overlap(ctypes.byref(s), p, p, 0, p, None) == INVALID
+    assert L.td_index_overlap(ctypes.byref(s), ctypes.c_void_p(258), p, 8, p, None) == INVALID
+    assert L.td_index_overlap(ctypes.byref(shape(head_dim=64)), p, p, 8, p, None) == UNSUPPORTED

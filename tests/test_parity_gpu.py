@@ -285,8 +285,11 @@ def _tiny_inputs():
     return wl, layers
 
 
-def test_decode_step_tiny_matches_oracle(orc):
+@pytest.mark.parametrize("schedule", ["figure2", "per_layer_select"])
+def test_decode_step_tiny_matches_oracle(orc, schedule):
     wl, layers = _tiny_inputs()
+    if schedule == "per_layer_select":     # selection at every layer after the first two
+        wl = wl.with_(modes=W.per_layer_select_schedule(wl.layers))
     lens = W.seq_lens(wl)
     shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len,
                           scale=td.default_scale(D))
@@ -399,3 +402,52 @@ def test_cluster_and_global_split_merges_agree(orc, sparse):
         check_outputs(out, out32, ref, f"merge mode {mode}")
     rowmax = res[-1][1].abs().amax(dim=-1, keepdim=True).clamp_min(1e-6)
     assert ((res[1][1] - res[-1][1]).abs() / rowmax).max().item() <= 2e-6
+
+
+def _sorted_sets(rs, rows, k, n, short_every=3):
+    out = np.full((rows, k), -1, np.int32)
+    for r in range(rows):
+        m = k if r % short_every else rs.randint(0, k + 1)       # some rows shorter than k
+        out[r, :m] = np.sort(rs.choice(n, m, replace=False))
+    return out
+
+
+@pytest.mark.parametrize("k,n", [(1, 4), (7, 20), (512, 10240), (4096, 102400), (4096, 5000)])
+def test_index_overlap_random_sets(orc, k, n):
+    rs = np.random.RandomState(k + n)
+    B, Hkv = 3, 4
+    shape = td.make_shape(B, Hkv, Hkv, max(n, k))
+    a = _sorted_sets(rs, B * Hkv, k, n)
+    b = _sorted_sets(rs, B * Hkv, k, n)
+    b[0] = a[0]                                                   # identical row
+    counts = torch.full((B, Hkv), -5, dtype=torch.int32, device="cuda")
+    td.td_index_overlap(shape, torch.as_tensor(a).cuda(), torch.as_tensor(b).cuda(), k, counts)
+    got = counts.cpu().numpy().reshape(-1)
+    want = [orc.index_overlap(a[r], b[r]) for r in range(B * Hkv)]
+    assert got.tolist() == want
+
+
+def test_index_overlap_of_consecutive_selection_layers(orc):
+    """Figure 4(a)'s measure on a workload: the sets two selection layers pick
+    (through the library) overlap as the oracle counts them."""
+    wl = W.WORKLOADS["llama2-7b-10k"].with_(max_seq_len=2048, top_k=128)
+    lens = W.seq_lens(wl)
+    heavy = W.heavy_positions(wl)
+    shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len,
+                          scale=td.default_scale(D))
+    seq = torch.as_tensor(lens).cuda()
+    sets = []
+    for layer in (1, 2):
+        q, K, V = W.generate_layer(wl, layer, torch.device("cuda"), heavy[layer])
+        idx = torch.full((wl.batch, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device="cuda")
+        out = torch.empty_like(q)
+        td.td_full_attn_select(shape, q, K, V, seq, wl.top_k, idx, out, None, None,
+                               td.Workspace(shape, wl.top_k))
+        sets.append(idx)
+    counts = torch.empty((wl.batch, wl.kv_heads), dtype=torch.int32, device="cuda")
+    td.td_index_overlap(shape, sets[0], sets[1], wl.top_k, counts)
+    a, b = sets[0].cpu().numpy().reshape(-1, wl.top_k), sets[1].cpu().numpy().reshape(-1, wl.top_k)
+    assert counts.cpu().numpy().reshape(-1).tolist() == [orc.index_overlap(a[r], b[r])
+                                                        for r in range(len(a))]
+    # the planted heavy positions are shared by the layers: most of each set recurs
+    assert counts.float().mean().item() > 0.5 * wl.top_k

@@ -68,3 +68,9 @@ def test_random_index_sets():
     for row in idx.reshape(-1, 16):
         live = row[row >= 0]
         assert np.all(np.diff(live) > 0)
+
+
+def test_per_layer_select_schedule():
+    assert W.per_layer_select_schedule(5) == (W.FULL, W.FULL, W.FULL_SELECT, W.FULL_SELECT,
+                                              W.FULL_SELECT)
+    assert W.per_layer_select_schedule(32).count(W.FULL_SELECT) == 30

@@ -52,6 +52,14 @@ def all_full_schedule(num_layers: int) -> tuple[int, ...]:
     return tuple([FULL] * num_layers)
 
 
+def per_layer_select_schedule(num_layers: int) -> tuple[int, ...]:
+    """Token selection at every layer after the first two: the schedule whose
+    selection cost the review compares PPSA against (per-layer selection as in
+    Quest, §三 complexity comparison: L selections per step instead of 2).
+    With these kernels every such layer pays full attention plus the top-k."""
+    return tuple([FULL] * min(2, num_layers) + [FULL_SELECT] * max(0, num_layers - 2))
+
+
 # Optimal re-selection ("middle") layer per model family, TidalDecode review
 # §五 table: LLaMA-2-7B (LongChat, Yarn) -> L7, LLaMA-3-8B / 3.1-8B -> L14.
 RESELECTION_LAYER = {"llama-2-7b": 7, "llama-3-8b": 14}
