@@ -241,6 +241,43 @@ td_status td_plan_launch(td_plan *plan, void *stream);
 void td_plan_destroy(td_plan *plan);
 
 /*
+ * KV append: the decode step's new token joins each layer's cache before
+ * that layer attends (the growing KV cache of the decode phase, review §二).
+ * seq_lens[b] already counts the new token, which sits at position
+ * p_b = seq_lens[b] - 1.
+ *   k_new, v_new   device bf16 [B][Hkv][128]: the new token's K and V rows
+ *                  (16-byte aligned).
+ *
+ * td_kv_append writes k_new/v_new into k_cache/v_cache at p_b (rows with
+ * seq_lens[b] outside [1, max_seq_len] are left alone).
+ *
+ * td_decode_step_append / td_plan_create_append: td_decode_step /
+ * td_plan_create plus, per layer l, k_new[l] / v_new[l] (HOST arrays of
+ * num_layers device pointers, both NULL for no append).  Each layer's
+ * attention kernel writes its layer's new rows into the cache itself and
+ * uses them for position p_b (full layers attend to it; a sparse layer uses
+ * it when p_b is in the persisted set), so the step needs no extra launch.
+ * The result equals td_kv_append on every layer followed by td_decode_step.
+ * k_new/v_new may be written by the kernel just before the call.
+ */
+td_status td_kv_append(const td_shape *shape, void *k_cache, void *v_cache, const void *k_new,
+                       const void *v_new, const int32_t *seq_lens, void *stream);
+td_status td_decode_step_append(const td_shape *shape, int32_t num_layers, const int32_t *modes,
+                                const void *const *q, const void *const *k_caches,
+                                const void *const *v_caches, const void *const *k_new,
+                                const void *const *v_new, const int32_t *seq_lens,
+                                int32_t top_k, int32_t *idx_buf, int32_t idx_valid,
+                                void *const *outs, float *const *outs_f32, void *ws,
+                                size_t ws_bytes, void *stream, void *const *layer_events);
+td_status td_plan_create_append(td_plan **plan, const td_shape *shape, int32_t num_layers,
+                                const int32_t *modes, const void *const *q,
+                                const void *const *k_caches, const void *const *v_caches,
+                                const void *const *k_new, const void *const *v_new,
+                                const int32_t *seq_lens, int32_t top_k, int32_t *idx_buf,
+                                int32_t idx_valid, void *const *outs, float *const *outs_f32,
+                                void *ws, size_t ws_bytes);
+
+/*
  * Kernel tuning knobs (process-wide, not thread-safe; for sweeps):
  *   "full_ctas_per_sm", "sparse_ctas_per_sm": resident CTAs assumed per SM
  *   "full_waves", "sparse_waves": target waves of CTAs per launch

@@ -75,6 +75,14 @@ def lib():
     L.td_full_attn_select.argtypes = [shp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
     L.td_topk_select.restype = ctypes.c_int
     L.td_topk_select.argtypes = [shp, vp, vp, i32, vp, vp, sz, vp]
+    L.td_kv_append.restype = ctypes.c_int
+    L.td_kv_append.argtypes = [shp, vp, vp, vp, vp, vp, vp]
+    L.td_decode_step_append.restype = ctypes.c_int
+    L.td_decode_step_append.argtypes = [shp, i32, vp, vpp, vpp, vpp, vpp, vpp, vp, i32, vp, i32,
+                                        vpp, vpp, vp, sz, vp, vpp]
+    L.td_plan_create_append.restype = ctypes.c_int
+    L.td_plan_create_append.argtypes = [ctypes.POINTER(vp), shp, i32, vp, vpp, vpp, vpp, vpp, vpp,
+                                        vp, i32, vp, i32, vpp, vpp, vp, sz]
     L.td_index_overlap.restype = ctypes.c_int
     L.td_index_overlap.argtypes = [shp, vp, vp, i32, vp, vp]
     L.td_sparse_attn.restype = ctypes.c_int
@@ -255,7 +263,7 @@ class _StepArgs:
     """Marshalled arguments of one decode step (kept alive while in use)."""
 
     def __init__(self, shape, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf, outs,
-                 outs_f32):
+                 outs_f32, k_new=None, v_new=None):
         nq, nkv, nb = _sizes(shape)
         L = len(modes)
         if not (len(q) == len(k_caches) == len(v_caches) == len(outs) == L):
@@ -275,12 +283,35 @@ class _StepArgs:
         self.idx = _dev(idx_buf, "idx_buf", torch.int32, nb * shape.num_kv_heads * top_k,
                         optional=not needs_idx)
         self.top_k = int(top_k)
+        if (k_new is None) != (v_new is None):
+            raise ValueError("k_new and v_new go together")
+        self.append = k_new is not None
+        if self.append:
+            if not (len(k_new) == len(v_new) == L):
+                raise ValueError("k_new / v_new need one entry per mode")
+            n_new = nb * shape.num_kv_heads * shape.head_dim
+            self.k_new = _ptr_array(k_new, "k_new", torch.bfloat16, n_new)
+            self.v_new = _ptr_array(v_new, "v_new", torch.bfloat16, n_new)
+
+
+def td_kv_append(shape: Shape, k_cache, v_cache, k_new, v_new, seq_lens, stream=None):
+    nq, nkv, nb = _sizes(shape)
+    n_new = nb * shape.num_kv_heads * shape.head_dim
+    st = lib().td_kv_append(
+        ctypes.byref(shape), _dev(k_cache, "k_cache", torch.bfloat16, nkv),
+        _dev(v_cache, "v_cache", torch.bfloat16, nkv), _dev(k_new, "k_new", torch.bfloat16, n_new),
+        _dev(v_new, "v_new", torch.bfloat16, n_new), _dev(seq_lens, "seq_lens", torch.int32, nb),
+        _stream(stream))
+    _check(st, "td_kv_append")
 
 
 def td_decode_step(shape: Shape, modes: Sequence[int], q, k_caches, v_caches, seq_lens, top_k,
                    idx_buf, outs, outs_f32=None, ws: Workspace = None, idx_valid=False,
-                   stream=None, layer_events: Optional[Sequence] = None):
-    a = _StepArgs(shape, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf, outs, outs_f32)
+                   stream=None, layer_events: Optional[Sequence] = None, k_new=None, v_new=None):
+    """One decode step; with k_new / v_new (per-layer [B][Hkv][128] rows) the
+    step also appends the new token to each layer's cache (td_decode_step_append)."""
+    a = _StepArgs(shape, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf, outs, outs_f32,
+                  k_new, v_new)
     ev = None
     if layer_events is not None:
         if len(layer_events) != a.L + 1:
@@ -289,6 +320,12 @@ def td_decode_step(shape: Shape, modes: Sequence[int], q, k_caches, v_caches, se
             if int(e.cuda_event) == 0:   # torch creates the CUDA event on first record
                 e.record(_torch_stream(stream))
         ev =(ctypes.c_void_p * (a.L + 1))(*[int(e.cuda_event) for e in layer_events])
+    if a.append:
+        st = lib().td_decode_step_append(ctypes.byref(shape), a.L, a.modes, a.q, a.k, a.v, a.k_new,
+                                         a.v_new, a.seq, a.top_k, a.idx, int(bool(idx_valid)),
+                                         a.outs, a.outs_f32, ws.ptr, ws.nbytes, _stream(stream), ev)
+        _check(st, "td_decode_step_append")
+        return
     st = lib().td_decode_step(ctypes.byref(shape), a.L, a.modes, a.q, a.k, a.v, a.seq, a.top_k,
                               a.idx, int(bool(idx_valid)), a.outs, a.outs_f32, ws.ptr, ws.nbytes,
                               _stream(stream), ev)
@@ -299,12 +336,19 @@ class Plan:
     """A decode step captured once into a CUDA graph (td_plan_create)."""
 
     def __init__(self, shape: Shape, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf, outs,
-                 outs_f32=None, ws: Workspace = None, idx_valid=False):
+                 outs_f32=None, ws: Workspace = None, idx_valid=False, k_new=None, v_new=None):
         self._args = _StepArgs(shape, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf,
-                               outs, outs_f32)
-        self._keep = (q, k_caches, v_caches, seq_lens, idx_buf, outs, outs_f32, ws)
+                               outs, outs_f32, k_new, v_new)
+        self._keep = (q, k_caches, v_caches, seq_lens, idx_buf, outs, outs_f32, ws, k_new, v_new)
         self._plan = ctypes.c_void_p(0)
         a = self._args
+        if a.append:
+            st = lib().td_plan_create_append(
+                ctypes.byref(self._plan), ctypes.byref(shape), a.L, a.modes, a.q, a.k, a.v,
+                a.k_new, a.v_new, a.seq, a.top_k, a.idx, int(bool(idx_valid)), a.outs, a.outs_f32,
+                ws.ptr, ws.nbytes)
+            _check(st, "td_plan_create_append")
+            return
         st = lib().td_plan_create(ctypes.byref(self._plan), ctypes.byref(shape), a.L, a.modes,
                                   a.q, a.k, a.v, a.seq, a.top_k, a.idx, int(bool(idx_valid)),
                                   a.outs, a.outs_f32, ws.ptr, ws.nbytes)

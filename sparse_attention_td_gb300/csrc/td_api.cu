@@ -264,19 +264,29 @@ td_status check_layer_ptrs(const void *q, const void *k, const void *v, const vo
     return TD_OK;
 }
 
-// Launches of one full(+select) layer; arguments already validated.
-td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
+// The new K/V rows of one layer (KV append), or none.
+struct Append {
+    const void *k_new = nullptr;
+    const void *v_new = nullptr;
+};
+
+// Launches of one full(+select) layer; arguments already validated.  pdl: the
+// attention kernel follows a kernel of the same call (programmatic dependent
+// launch); the first kernel of a call is ordered by the stream alone.
+td_status run_full(const Ctx &c, const void *q, const void *k, const void *v, Append ap,
                    const int32_t *seq_lens, int top_k, int32_t *idx_out, void *out,
-                   float *out_f32, float *scores_out, cudaStream_t st)
+                   float *out_f32, float *scores_out, cudaStream_t st, bool pdl)
 {
     const bool select = top_k > 0;
     td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
+    a.k_new = (const uint16_t *)ap.k_new;
+    a.v_new = (const uint16_t *)ap.v_new;
     a.scores = select ? (scores_out ? scores_out : (float *)(c.wsb + c.ws.scores)) : nullptr;
     a.hist = select ? (unsigned *)(c.wsb + c.ws.hist) : nullptr;
     plan_splits(c.shape, c.shape.max_seq_len, false, select, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
-    if (td::launch_attention(c.G, false, select, cluster, staged_for(false, c.G), a, c.shape.batch, st) !=
-        cudaSuccess)
+    if (td::launch_attention(c.G, false, select, cluster, staged_for(false, c.G), a, c.shape.batch,
+                             pdl, st) != cudaSuccess)
         return TD_ERR_CUDA;
     if (select) {
         td::TopkArgs t{};
@@ -288,7 +298,7 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
         t.Hkv = c.shape.num_kv_heads;
         t.Nmax = c.shape.max_seq_len;
         t.top_k = top_k;
-        if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, st) != cudaSuccess)
+        if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, true, st) != cudaSuccess)
             return TD_ERR_CUDA;
     }
     return TD_OK;
@@ -296,18 +306,20 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
 
 // idx_dep: the kernel launched just before may have written `idx` (then the
 // sparse kernel waits for it before reading the set).
-td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
+td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v, Append ap,
                      const int32_t *seq_lens, const int32_t *idx, int top_k, void *out,
-                     float *out_f32, cudaStream_t st, bool idx_dep)
+                     float *out_f32, cudaStream_t st, bool idx_dep, bool pdl)
 {
     td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
+    a.k_new = (const uint16_t *)ap.k_new;
+    a.v_new = (const uint16_t *)ap.v_new;
     a.idx = idx;
     a.top_k = top_k;
     a.idx_dep = idx_dep ? 1 : 0;
     plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
-    if (td::launch_attention(c.G, true, false, cluster, staged_for(true, c.G), a, c.shape.batch, st) !=
-        cudaSuccess)
+    if (td::launch_attention(c.G, true, false, cluster, staged_for(true, c.G), a, c.shape.batch, pdl,
+                             st) != cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }
@@ -316,9 +328,12 @@ td_status validate_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
                         const void *const *q, const void *const *k_caches,
                         const void *const *v_caches, const int32_t *seq_lens, int32_t top_k,
                         const int32_t *idx_buf, int32_t idx_valid, void *const *outs,
-                        float *const *outs_f32)
+                        float *const *outs_f32, const void *const *k_new,
+                        const void *const *v_new)
 {
     (void)c;
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return TD_ERR_INVALID_ARG;
     if (num_layers < 0 || (num_layers > 0 && (!modes || !q || !k_caches || !v_caches || !outs)))
         return TD_ERR_INVALID_ARG;
     if (!seq_lens || !aligned(seq_lens, 4))
@@ -333,6 +348,8 @@ td_status validate_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
                                         outs_f32 ? outs_f32[l] : nullptr);
         if (st)
             return st;
+        if (k_new && (!k_new[l] || !v_new[l] || !aligned(k_new[l], 16) || !aligned(v_new[l], 16)))
+            return TD_ERR_INVALID_ARG;
         if (m == TD_MODE_FULL_SELECT) {
             if (top_k < 1)
                 return TD_ERR_INVALID_ARG;
@@ -355,9 +372,16 @@ td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
                        const void *const *q, const void *const *k_caches,
                        const void *const *v_caches, const int32_t *seq_lens, int32_t top_k,
                        int32_t *idx_buf, void *const *outs, float *const *outs_f32,
-                       cudaStream_t st, void *const *layer_events)
+                       const void *const *k_new, const void *const *v_new, cudaStream_t st,
+                       void *const *layer_events)
 {
     for (int l = 0; l < num_layers; ++l) {
+        Append ap;
+        if (k_new) {
+            ap.k_new = k_new[l];
+            ap.v_new = v_new[l];
+        }
+        const bool pdl = l > 0;  // the first kernel waits for whatever precedes the call
         if (layer_events && layer_events[l] &&
             cudaEventRecord((cudaEvent_t)layer_events[l], st) != cudaSuccess)
             return TD_ERR_CUDA;
@@ -365,16 +389,16 @@ td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
         td_status r;
         switch (modes[l]) {
         case TD_MODE_FULL:
-            r = run_full(c, q[l], k_caches[l], v_caches[l], seq_lens, 0, nullptr, outs[l], of,
-                         nullptr, st);
+            r = run_full(c, q[l], k_caches[l], v_caches[l], ap, seq_lens, 0, nullptr, outs[l], of,
+                         nullptr, st, pdl);
             break;
         case TD_MODE_FULL_SELECT:
-            r = run_full(c, q[l], k_caches[l], v_caches[l], seq_lens, top_k, idx_buf, outs[l],
-                         of, nullptr, st);
+            r = run_full(c, q[l], k_caches[l], v_caches[l], ap, seq_lens, top_k, idx_buf,
+                         outs[l], of, nullptr, st, pdl);
             break;
         default:
-            r = run_sparse(c, q[l], k_caches[l], v_caches[l], seq_lens, idx_buf, top_k, outs[l],
-                           of, st, l == 0 || modes[l - 1] == TD_MODE_FULL_SELECT);
+            r = run_sparse(c, q[l], k_caches[l], v_caches[l], ap, seq_lens, idx_buf, top_k,
+                           outs[l], of, st, l == 0 || modes[l - 1] == TD_MODE_FULL_SELECT, pdl);
             break;
         }
         if (r)
@@ -457,8 +481,8 @@ td_status td_full_attn_select(const td_shape *shape, const void *q, const void *
         return TD_ERR_INVALID_ARG;
     if (scores_out && !aligned(scores_out, 4))
         return TD_ERR_INVALID_ARG;
-    return run_full(c, q, k_cache, v_cache, seq_lens, top_k, idx_out, out, out_f32,
-                    top_k > 0 ? scores_out : nullptr, (cudaStream_t)stream);
+    return run_full(c, q, k_cache, v_cache, Append{}, seq_lens, top_k, idx_out, out, out_f32,
+                    top_k > 0 ? scores_out : nullptr, (cudaStream_t)stream, false);
 }
 
 td_status td_topk_select(const td_shape *shape, const float *scores, const int32_t *seq_lens,
@@ -480,7 +504,8 @@ td_status td_topk_select(const td_shape *shape, const float *scores, const int32
     t.Hkv = c.shape.num_kv_heads;
     t.Nmax = c.shape.max_seq_len;
     t.top_k = top_k;
-    if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, (cudaStream_t)stream) != cudaSuccess)
+    if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, false, (cudaStream_t)stream) !=
+        cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }
@@ -515,8 +540,8 @@ td_status td_sparse_attn(const td_shape *shape, const void *q, const void *k_cac
         return st;
     if (top_k < 1 || !idx || !aligned(idx, 4) || !seq_lens || !aligned(seq_lens, 4))
         return TD_ERR_INVALID_ARG;
-    return run_sparse(c, q, k_cache, v_cache, seq_lens, idx, top_k, out, out_f32,
-                      (cudaStream_t)stream, true);
+    return run_sparse(c, q, k_cache, v_cache, Append{}, seq_lens, idx, top_k, out, out_f32,
+                      (cudaStream_t)stream, true, false);
 }
 
 td_status td_decode_step(const td_shape *shape, int32_t num_layers, const int32_t *modes,
@@ -526,16 +551,47 @@ td_status td_decode_step(const td_shape *shape, int32_t num_layers, const int32_
                          float *const *outs_f32, void *ws, size_t ws_bytes, void *stream,
                          void *const *layer_events)
 {
+    return td_decode_step_append(shape, num_layers, modes, q, k_caches, v_caches, nullptr,
+                                 nullptr, seq_lens, top_k, idx_buf, idx_valid, outs, outs_f32, ws,
+                                 ws_bytes, stream, layer_events);
+}
+
+td_status td_decode_step_append(const td_shape *shape, int32_t num_layers, const int32_t *modes,
+                                const void *const *q, const void *const *k_caches,
+                                const void *const *v_caches, const void *const *k_new,
+                                const void *const *v_new, const int32_t *seq_lens,
+                                int32_t top_k, int32_t *idx_buf, int32_t idx_valid,
+                                void *const *outs, float *const *outs_f32, void *ws,
+                                size_t ws_bytes, void *stream, void *const *layer_events)
+{
     Ctx c;
     td_status st = make_ctx(shape, top_k, ws, ws_bytes, c);
     if (st)
         return st;
     st = validate_step(c, num_layers, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf,
-                       idx_valid, outs, outs_f32);
+                       idx_valid, outs, outs_f32, k_new, v_new);
     if (st)
         return st;
     return enqueue_step(c, num_layers, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf,
-                        outs, outs_f32, (cudaStream_t)stream, layer_events);
+                        outs, outs_f32, k_new, v_new, (cudaStream_t)stream, layer_events);
+}
+
+td_status td_kv_append(const td_shape *shape, void *k_cache, void *v_cache, const void *k_new,
+                       const void *v_new, const int32_t *seq_lens, void *stream)
+{
+    td_status st = check_shape(shape);
+    if (st)
+        return st;
+    if (!k_cache || !v_cache || !k_new || !v_new || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !seq_lens ||
+        !aligned(seq_lens, 4))
+        return TD_ERR_INVALID_ARG;
+    if (td::launch_kv_append((uint16_t *)k_cache, (uint16_t *)v_cache, (const uint16_t *)k_new,
+                             (const uint16_t *)v_new, seq_lens, shape->batch,
+                             shape->num_kv_heads, shape->max_seq_len, (cudaStream_t)stream) !=
+        cudaSuccess)
+        return TD_ERR_CUDA;
+    return TD_OK;
 }
 
 td_status td_plan_create(td_plan **plan, const td_shape *shape, int32_t num_layers,
@@ -545,6 +601,19 @@ td_status td_plan_create(td_plan **plan, const td_shape *shape, int32_t num_laye
                          int32_t idx_valid, void *const *outs, float *const *outs_f32, void *ws,
                          size_t ws_bytes)
 {
+    return td_plan_create_append(plan, shape, num_layers, modes, q, k_caches, v_caches, nullptr,
+                                 nullptr, seq_lens, top_k, idx_buf, idx_valid, outs, outs_f32, ws,
+                                 ws_bytes);
+}
+
+td_status td_plan_create_append(td_plan **plan, const td_shape *shape, int32_t num_layers,
+                                const int32_t *modes, const void *const *q,
+                                const void *const *k_caches, const void *const *v_caches,
+                                const void *const *k_new, const void *const *v_new,
+                                const int32_t *seq_lens, int32_t top_k, int32_t *idx_buf,
+                                int32_t idx_valid, void *const *outs, float *const *outs_f32,
+                                void *ws, size_t ws_bytes)
+{
     if (!plan)
         return TD_ERR_INVALID_ARG;
     *plan = nullptr;
@@ -553,7 +622,7 @@ td_status td_plan_create(td_plan **plan, const td_shape *shape, int32_t num_laye
     if (st)
         return st;
     st = validate_step(c, num_layers, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf,
-                       idx_valid, outs, outs_f32);
+                       idx_valid, outs, outs_f32, k_new, v_new);
     if (st)
         return st;
     td_plan *p = new (std::nothrow) td_plan();
@@ -569,7 +638,7 @@ td_status td_plan_create(td_plan **plan, const td_shape *shape, int32_t num_laye
         st = TD_ERR_CUDA;
     } else {
         td_status enq = enqueue_step(c, num_layers, modes, q, k_caches, v_caches, seq_lens,
-                                     top_k, idx_buf, outs, outs_f32, cap, nullptr);
+                                     top_k, idx_buf, outs, outs_f32, k_new, v_new, cap, nullptr);
         cudaGraph_t graph = nullptr;
         const cudaError_t end = cudaStreamEndCapture(cap, &graph);
         if (enq != TD_OK || end != cudaSuccess) {

@@ -159,7 +159,7 @@ extern "C" td_status td_sparse_attn_noalloc(const td_shape *shape, const void *q
     a.chunk = chunk;
     a.nsplit = nsplit;
     a.scale = s.scale != 0.0f ? s.scale : 1.0f / sqrtf((float)s.head_dim);
-    if (td::launch_attention(G, true, false, false, false, a, s.batch, cs) != cudaSuccess)
+    if (td::launch_attention(G, true, false, false, false, a, s.batch, false, cs) != cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }

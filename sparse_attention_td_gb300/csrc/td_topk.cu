@@ -635,7 +635,7 @@ static_assert(kSubHists * kBins1 <= 2 * TopkCfg<512>::kCand, "pass-1 sub-histogr
 static_assert(2 * (topk_smem_bytes<512>() + 1024) <= 228 * 1024, "two 512-thread CTAs fit one SM");
 
 template <int NT>
-cudaError_t launch_topk_nt(const TopkArgs &a, int batch, cudaStream_t stream)
+cudaError_t launch_topk_nt(const TopkArgs &a, int batch, bool pdl, cudaStream_t stream)
 {
     constexpr size_t smem = topk_smem_bytes<NT>();
     static bool configured[64] = {false};  // the smem opt-in is per device
@@ -658,7 +658,7 @@ cudaError_t launch_topk_nt(const TopkArgs &a, int batch, cudaStream_t stream)
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, topk_kernel<NT>, a);
@@ -666,7 +666,8 @@ cudaError_t launch_topk_nt(const TopkArgs &a, int batch, cudaStream_t stream)
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, cudaStream_t stream)
+cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, bool pdl,
+                        cudaStream_t stream)
 {
     if (threads == 0) {  // one wave of 1024-thread CTAs if the rows fit, else 512-thread pairs
         int dev = 0, sms = 0;
@@ -677,8 +678,8 @@ cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, cudaStream_t 
             return e;
         threads = (long)a.Hkv * batch > sms ? 512 : 1024;
     }
-    return threads == 512 ? launch_topk_nt<512>(a, batch, stream)
-                          : launch_topk_nt<1024>(a, batch, stream);
+    return threads == 512 ? launch_topk_nt<512>(a, batch, pdl, stream)
+                          : launch_topk_nt<1024>(a, batch, pdl, stream);
 }
 
 }  // namespace td
