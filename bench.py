@@ -246,6 +246,38 @@ def consecutive_overlap(td, torch, wl, shape, q, K, V, seq, ws, device):
             "layers": f"2..{wl.layers - 1}"}
 
 
+def coverage_layer(td, torch, wl, shape, q, K, V, seq, ws, device, flush_l2, stream,
+                   tau=0.1, reps=20):
+    """One selection layer (layer 2) with a coverage budget (tau, at most top_k
+    positions) against the same layer with top-k: launch times (events, L2
+    flushed before each launch) and the mean budget chosen."""
+    idx = torch.full((wl.batch, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device=device)
+    counts = torch.empty((wl.batch, wl.kv_heads), dtype=torch.int32, device=device)
+    out = torch.empty_like(q[2])
+
+    def timed(fn):
+        ev = []
+        for i in range(reps + 3):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            if i >= 3:
+                ev.append((a, b))
+        torch.cuda.synchronize(device)
+        return statistics.fmean(a.elapsed_time(b) for a, b in ev) * 1e3
+
+    t_cov = timed(lambda: td.td_full_attn_select_coverage(
+        shape, q[2], K[2], V[2], seq, tau, wl.top_k, idx, counts, out, None, None, ws,
+        stream=stream))
+    t_topk = timed(lambda: td.td_full_attn_select(shape, q[2], K[2], V[2], seq, wl.top_k, idx, out,
+                                                  None, None, ws, stream=stream))
+    return {"tau": tau, "k_max": wl.top_k, "layer_us": round(t_cov, 2),
+            "top_k_layer_us": round(t_topk, 2),
+            "mean_budget": round(float(counts.to(torch.float32).mean().item()), 1)}
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args, world, rank, local):
     import torch
@@ -278,6 +310,15 @@ def run_ours(args, world, rank, local):
     plan = td.Plan(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
     plan_full = td.Plan(shape, full_modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
     plan_sel = td.Plan(shape, sel_modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
+    # the same PPSA step with the new token's K/V rows appended to every layer's
+    # cache by the attention kernels themselves (rewrites position N_b - 1)
+    gen = torch.Generator(device=device).manual_seed(wl.seed + 77)
+    k_new = [torch.randn(wl.batch, wl.kv_heads, wl.head_dim, generator=gen, device=device)
+             .to(torch.bfloat16) for _ in range(wl.layers)]
+    v_new = [torch.randn(wl.batch, wl.kv_heads, wl.head_dim, generator=gen, device=device)
+             .to(torch.bfloat16) for _ in range(wl.layers)]
+    plan_app = td.Plan(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws,
+                       k_new=k_new, v_new=v_new)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     K_steps, W_steps = args.steps, args.warmup
@@ -303,6 +344,8 @@ def run_ours(args, world, rank, local):
         plan_full.launch(stream)
         flush_l2()
         plan_sel.launch(stream)
+        flush_l2()
+        plan_app.launch(stream)
         td.td_decode_step(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws,
                           stream=stream)
     torch.cuda.synchronize(device)
@@ -322,6 +365,9 @@ def run_ours(args, world, rank, local):
         ev_sel = graph_pass(plan_sel, K_steps)
         torch.cuda.synchronize(device)
         dist_barrier(world, device)
+        ev_app = graph_pass(plan_app, K_steps)
+        torch.cuda.synchronize(device)
+        dist_barrier(world, device)
         # pass 2: per-layer events around each layer's launches
         traced = []
         for _ in range(K_steps):
@@ -335,6 +381,7 @@ def run_ours(args, world, rank, local):
     ppsa_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_ppsa) * 1e3
     full_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_full) * 1e3
     sel_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_sel) * 1e3
+    app_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_app) * 1e3
     per_layer = np.array([[e[i].elapsed_time(e[i + 1]) * 1e3 for i in range(wl.layers)]
                           for e in traced])                      # [K, L] us
     traced_step_us = float(np.mean([e[0].elapsed_time(e[-1]) * 1e3 for e in traced]))
@@ -347,10 +394,12 @@ def run_ours(args, world, rank, local):
     ppsa_us = dist_max(ppsa_us, world, device)
     full_us = dist_max(full_us, world, device)
     sel_us = dist_max(sel_us, world, device)
+    app_us = dist_max(app_us, world, device)
 
     # Figure 4(a)'s measure on this data (untimed): the top-k set each layer
     # would select, and its overlap with the next layer's
     overlap = consecutive_overlap(td, torch, wl, shape, q, K, V, seq, ws, device)
+    coverage = coverage_layer(td, torch, wl, shape, q, K, V, seq, ws, device, flush_l2, stream)
 
     # e2e: host q in (pinned), graph step, host outputs back, per step
     q_host = [x.cpu().pin_memory() for x in q]
@@ -450,6 +499,8 @@ def run_ours(args, world, rank, local):
             "per_layer_select_us": round(sel_us, 2),
             "speedup_vs_per_layer_select": round(sel_us / ppsa_us, 3),
             "consecutive_layer_overlap": overlap,
+            "append_step_us": round(app_us, 2),
+            "coverage_selection": coverage,
             "traced_step_us": round(traced_step_us, 2),
             "layer_us": {k: round(v, 2) for k, v in by_mode.items()},
             "sparse_layer_gbs": round(sparse_gbs, 1) if sparse_gbs else None,

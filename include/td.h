@@ -134,6 +134,30 @@ td_status td_topk_select(const td_shape *shape, const float *scores, const int32
                          void *stream);
 
 /*
+ * A selection layer with a coverage budget instead of a fixed k ("Dynamic
+ * Token Coverage", Token Sparse Attention §2: rank the tokens by importance
+ * and prune the least important while the pruned attention mass stays within
+ * tau).  Full attention as td_full_attn_select; then per (batch row, KV
+ * head), with s the selection scores over the row's N_b positions:
+ *   k = min(k_max, the smallest k whose k highest scores hold at least 1 - tau
+ *       of softmax(s)),
+ * and the k positions with the highest scores (ties to the lower position)
+ * are written ascending to idx_out[b][g][0..k), the rest of the row -1.
+ *   tau in [0, 1); k_max >= 1 is the row length of idx_out [B][Hkv][k_max]
+ *   (size the workspace with td_workspace_size(shape, k_max)).
+ *   counts_out: device int32 [B][Hkv] (optional): k per row.
+ * The mass sums are fp32: where the cumulative mass at the cut is within
+ * rounding of 1 - tau, k may differ by one from an exact computation.  For
+ * grouped-query heads s is the summed logit of the group (as for top-k), so
+ * the mass is that of softmax over the summed logits.
+ */
+td_status td_full_attn_select_coverage(const td_shape *shape, const void *q, const void *k_cache,
+                                       const void *v_cache, const int32_t *seq_lens, float tau,
+                                       int32_t k_max, int32_t *idx_out, int32_t *counts_out,
+                                       void *out, float *out_f32, float *scores_out, void *ws,
+                                       size_t ws_bytes, void *stream);
+
+/*
  * Overlap of two index sets, per (batch row, KV head): counts[b][g] =
  * |A[b][g] ∩ B[b][g]|, the number of positions present in both.  This is the
  * measure behind the review's token-selection sensitivity analysis (§三

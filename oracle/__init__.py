@@ -113,6 +113,8 @@ class Oracle:
                                                               vpp, vpp, vpp, vpp, i32p]
         L.oracle_index_overlap.restype = ctypes.c_int
         L.oracle_index_overlap.argtypes = [i32p, i32p, ctypes.c_int]
+        L.oracle_coverage_count.restype = ctypes.c_int
+        L.oracle_coverage_count.argtypes = [f64p, ctypes.c_int, ctypes.c_double, ctypes.c_int]
         L.oracle_mutant_id.restype = ctypes.c_int
         L.oracle_num_threads.restype = ctypes.c_int
 
@@ -233,6 +235,15 @@ class Oracle:
         assert a.shape == b.shape and a.ndim == 1
         return int(self._lib.oracle_index_overlap(_ptr(a, ctypes.c_int32), _ptr(b, ctypes.c_int32),
                                                len(a)))
+
+    def coverage_count(self, s, tau: float, k_max: int) -> int:
+        """Smallest k whose top-k scores hold >= 1 - tau of softmax(s), <= k_max."""
+        s = np.ascontiguousarray(s, dtype=np.float64)
+        k = self._lib.oracle_coverage_count(_ptr(s, ctypes.c_double), s.size, float(tau),
+                                            int(k_max))
+        if k < 0:
+            raise MemoryError("oracle_coverage_count")
+        return int(k)
 
     def mutant_id(self) -> int:
         return self._lib.oracle_mutant_id()

@@ -22,7 +22,9 @@
  *   - the per-step layer schedule [full | full+select | sparse]
  *     (review §三 Figure 2);
  *   - the overlap of two token sets (review §三, token-selection
- *     sensitivity, Figure 4(a)).
+ *     sensitivity, Figure 4(a));
+ *   - a coverage budget for the selection (Token Sparse Attention page, §2
+ *     "Dynamic Token Coverage").
  *
  * Readings where the page is silent (each also listed in the design notes):
  *   - "attention score" for selection is the scaled pre-softmax logit a;
@@ -406,6 +408,49 @@ int oracle_decode_step(int B, int Hq, int Hkv, int d, int Nmax, const int32_t *s
         }
     }
     return rc_all;
+}
+
+/*
+ * Coverage budget (Token Sparse Attention page, §2 "Dynamic Token Coverage":
+ * rank tokens by importance and prune the least important while the pruned
+ * attention mass stays within tau): the smallest k such that the k highest
+ * scores (ties: lower position first) hold at least 1 - tau of softmax(s)
+ * over s[0..n), capped at k_max; n if the sum never reaches it (rounding).
+ * Returns k, or -1 if memory runs out.
+ */
+int oracle_coverage_count(const double *s, int n, double tau, int k_max)
+{
+    if (n <= 0 || k_max <= 0)
+        return 0;
+    double *p = (double *)malloc(sizeof(double) * (size_t)n);
+    scored_pos *v = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
+    if (!p || !v) {
+        free(p);
+        free(v);
+        return -1;
+    }
+    oracle_softmax(s, n, p);
+    for (int t = 0; t < n; ++t) {
+        v[t].s = s[t];
+        v[t].pos = t;
+    }
+    qsort(v, (size_t)n, sizeof(scored_pos), by_score_desc_pos_asc);
+    double mass = 0.0;
+    int k = n;
+    for (int j = 0; j < n; ++j) {
+        mass += p[v[j].pos];
+        if (mass >= 1.0 - tau) {
+            k = j + 1;
+            break;
+        }
+    }
+#if ORACLE_MUTANT == 14
+    if (k > 1)
+        k -= 1; /* mutant: stops one token before the coverage is reached */
+#endif
+    free(p);
+    free(v);
+    return k < k_max ? k : k_max;
 }
 
 /*

@@ -75,6 +75,9 @@ def lib():
     L.td_full_attn_select.argtypes = [shp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
     L.td_topk_select.restype = ctypes.c_int
     L.td_topk_select.argtypes = [shp, vp, vp, i32, vp, vp, sz, vp]
+    L.td_full_attn_select_coverage.restype = ctypes.c_int
+    L.td_full_attn_select_coverage.argtypes = [shp, vp, vp, vp, vp, ctypes.c_float, i32, vp, vp,
+                                               vp, vp, vp, vp, sz, vp]
     L.td_kv_append.restype = ctypes.c_int
     L.td_kv_append.argtypes = [shp, vp, vp, vp, vp, vp, vp]
     L.td_decode_step_append.restype = ctypes.c_int
@@ -204,6 +207,22 @@ def td_full_attn_select(shape: Shape, q, k_cache, v_cache, seq_lens, top_k, idx_
         _dev(scores_out, "scores_out", torch.float32, nkv // shape.head_dim, True),
         ws.ptr, ws.nbytes, _stream(stream))
     _check(st, "td_full_attn_select")
+
+
+def td_full_attn_select_coverage(shape: Shape, q, k_cache, v_cache, seq_lens, tau, k_max, idx_out,
+                                 counts_out, out, out_f32=None, scores_out=None,
+                                 ws: Workspace = None, stream=None):
+    nq, nkv, nb = _sizes(shape)
+    st = lib().td_full_attn_select_coverage(
+        ctypes.byref(shape), _dev(q, "q", torch.bfloat16, nq),
+        _dev(k_cache, "k_cache", torch.bfloat16, nkv), _dev(v_cache, "v_cache", torch.bfloat16, nkv),
+        _dev(seq_lens, "seq_lens", torch.int32, nb), float(tau), int(k_max),
+        _dev(idx_out, "idx_out", torch.int32, nb * shape.num_kv_heads * k_max),
+        _dev(counts_out, "counts_out", torch.int32, nb * shape.num_kv_heads, True),
+        _dev(out, "out", torch.bfloat16, nq), _dev(out_f32, "out_f32", torch.float32, nq, True),
+        _dev(scores_out, "scores_out", torch.float32, nkv // shape.head_dim, True),
+        ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "td_full_attn_select_coverage")
 
 
 def td_topk_select(shape: Shape, scores, seq_lens, top_k, idx_out, ws: Workspace = None,

@@ -99,7 +99,7 @@ long partial_slots(const td_shape &s, int top_k)
 }
 
 struct WsLayout {
-    size_t status, tickets, part_m, part_l, part_o, scores, hist, total;
+    size_t status, tickets, part_m, part_l, part_o, scores, hist, row_k, total;
 };
 
 WsLayout ws_layout(const td_shape &s, int top_k)
@@ -125,6 +125,9 @@ WsLayout ws_layout(const td_shape &s, int top_k)
     w.hist = off;  // first-digit histograms of a selection layer (kept zero between uses)
     if (top_k > 0)
         off = align_up(off + units * (size_t)td::kSelectBins * sizeof(unsigned));
+    w.row_k = off;  // per-row budgets of a coverage selection
+    if (top_k > 0)
+        off = align_up(off + units * sizeof(int32_t));
     w.total = off;
     return w;
 }
@@ -273,9 +276,17 @@ struct Append {
 // Launches of one full(+select) layer; arguments already validated.  pdl: the
 // attention kernel follows a kernel of the same call (programmatic dependent
 // launch); the first kernel of a call is ordered by the stream alone.
+// Coverage selection (tau >= 0): a per-row budget instead of top_k for every
+// row; counts (optional) receives the number of positions kept per row.
+struct Coverage {
+    float tau = -1.0f;
+    int32_t *counts = nullptr;
+};
+
 td_status run_full(const Ctx &c, const void *q, const void *k, const void *v, Append ap,
                    const int32_t *seq_lens, int top_k, int32_t *idx_out, void *out,
-                   float *out_f32, float *scores_out, cudaStream_t st, bool pdl)
+                   float *out_f32, float *scores_out, cudaStream_t st, bool pdl,
+                   Coverage cov = Coverage{})
 {
     const bool select = top_k > 0;
     td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
@@ -298,6 +309,20 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v, Ap
         t.Hkv = c.shape.num_kv_heads;
         t.Nmax = c.shape.max_seq_len;
         t.top_k = top_k;
+        if (cov.tau >= 0.0f) {
+            td::CoverageArgs ca{};
+            ca.scores = a.scores;
+            ca.seq_lens = seq_lens;
+            ca.row_k = (int32_t *)(c.wsb + c.ws.row_k);
+            ca.Hkv = c.shape.num_kv_heads;
+            ca.Nmax = c.shape.max_seq_len;
+            ca.kcap = top_k;
+            ca.tau = cov.tau;
+            if (td::launch_coverage(ca, c.shape.batch, true, st) != cudaSuccess)
+                return TD_ERR_CUDA;
+            t.row_k = ca.row_k;
+            t.counts = cov.counts;
+        }
         if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, true, st) != cudaSuccess)
             return TD_ERR_CUDA;
     }
@@ -483,6 +508,30 @@ td_status td_full_attn_select(const td_shape *shape, const void *q, const void *
         return TD_ERR_INVALID_ARG;
     return run_full(c, q, k_cache, v_cache, Append{}, seq_lens, top_k, idx_out, out, out_f32,
                     top_k > 0 ? scores_out : nullptr, (cudaStream_t)stream, false);
+}
+
+td_status td_full_attn_select_coverage(const td_shape *shape, const void *q, const void *k_cache,
+                                       const void *v_cache, const int32_t *seq_lens, float tau,
+                                       int32_t k_max, int32_t *idx_out, int32_t *counts_out,
+                                       void *out, float *out_f32, float *scores_out, void *ws,
+                                       size_t ws_bytes, void *stream)
+{
+    Ctx c;
+    td_status st = make_ctx(shape, k_max, ws, ws_bytes, c);
+    if (st)
+        return st;
+    st = check_layer_ptrs(q, k_cache, v_cache, out, out_f32);
+    if (st)
+        return st;
+    if (!(tau >= 0.0f && tau < 1.0f) || k_max < 1 || !idx_out || !aligned(idx_out, 4) ||
+        !seq_lens || !aligned(seq_lens, 4) || (counts_out && !aligned(counts_out, 4)) ||
+        (scores_out && !aligned(scores_out, 4)))
+        return TD_ERR_INVALID_ARG;
+    Coverage cov;
+    cov.tau = tau;
+    cov.counts = counts_out;
+    return run_full(c, q, k_cache, v_cache, Append{}, seq_lens, k_max, idx_out, out, out_f32,
+                    scores_out, (cudaStream_t)stream, false, cov);
 }
 
 td_status td_topk_select(const td_shape *shape, const float *scores, const int32_t *seq_lens,

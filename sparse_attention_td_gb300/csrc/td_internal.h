@@ -61,7 +61,19 @@ struct TopkArgs {
     const int32_t *seq_lens; // [B]
     int32_t *idx;            // [B][Hkv][top_k]
     uint32_t *status;
+    const int32_t *row_k;    // [B*Hkv] per-row budget (<= top_k), or null: top_k for every row
+    int32_t *counts;         // [B*Hkv] positions selected per row (min(k, N_b)), or null
     int Hkv, Nmax, top_k;
+};
+
+// Coverage budget per (batch row, KV head): row_k[bg] = min(kcap, smallest k
+// whose top-k scores hold >= 1 - tau of softmax(scores) over the row).
+struct CoverageArgs {
+    const float *scores;     // [B][Hkv][Nmax]
+    const int32_t *seq_lens; // [B]
+    int32_t *row_k;          // [B*Hkv] out
+    int Hkv, Nmax, kcap;
+    float tau;
 };
 
 // G = query heads per KV head (1, 2, 4, 8).
@@ -79,6 +91,7 @@ cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, bool
 // one wave on the device's SMs, else 512 (two CTAs per SM).
 cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, bool pdl,
                         cudaStream_t stream);
+cudaError_t launch_coverage(const CoverageArgs &a, int batch, bool pdl, cudaStream_t stream);
 
 // KV append: rows k_new/v_new [B][Hkv][128] written at position seq_lens[b]-1.
 cudaError_t launch_kv_append(uint16_t *k, uint16_t *v, const uint16_t *k_new,

@@ -314,7 +314,7 @@ topk_kernel(const TopkArgs a)
     const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const size_t bg = (size_t)b * a.Hkv + g;
-    const int k = a.top_k;
+    const int kcap = a.top_k;  // row length of the output
     int n = a.seq_lens[b];
     if (n < 0 || n > a.Nmax) {
         if (tid == 0 && g == 0)
@@ -322,14 +322,21 @@ topk_kernel(const TopkArgs a)
         n = n < 0 ? 0 : a.Nmax;
     }
     const float *s = a.scores + bg * (size_t)a.Nmax;
-    int32_t *out = a.idx + bg * (size_t)k;
+    int32_t *out = a.idx + bg * (size_t)kcap;
     pdl_wait();
     pdl_launch_dependents();
+    int k = kcap;  // positions to select in this row (a per-row budget, at most kcap)
+    if (a.row_k) {
+        const int rk = __ldcg(a.row_k + bg);
+        k = rk < 0 ? 0 : (rk < kcap ? rk : kcap);
+    }
+    if (a.counts && tid == 0)
+        a.counts[bg] = k < n ? k : n;
 
     unsigned *ghist = a.hist ? a.hist + bg * kBins1 : nullptr;
-    if (n <= k) {  // every position is kept
-        for (int j = tid; j < k; j += kT)
-            out[j] = j < n ? j : -1;
+    if (n <= k || k == 0) {  // every position is kept, or none
+        for (int j = tid; j < kcap; j += kT)
+            out[j] = (j < n && j < k) ? j : -1;
         if (ghist)
             for (int i = tid; i < kBins1; i += kT)
                 ghist[i] = 0u;  // leave the fused histogram zero for the next selection
@@ -547,6 +554,8 @@ topk_kernel(const TopkArgs a)
                     ++slot;
                 }
             }
+            for (int j = k + tid; j < kcap; j += kT)
+                out[j] = -1;  // a per-row budget below the row length
             return;
         }
     } else {
@@ -623,6 +632,199 @@ topk_kernel(const TopkArgs a)
         out_base += sm.res[0];
         __syncthreads();
     }
+    for (int j = k + tid; j < kcap; j += kT)
+        out[j] = -1;  // a per-row budget below the row length
+}
+
+// ---------------------------------------------------------------------------
+// Coverage budget ("Dynamic Token Coverage", Token Sparse Attention §2: sort
+// the tokens by importance and prune the least important ones while their
+// cumulative attention mass stays within tau).  Per (batch row, KV head): the
+// smallest k such that the k highest-scoring positions hold at least 1 - tau
+// of softmax(s) over the row's N_b scores (ties: lower positions first), then
+// min(k, kcap).  Mass is reduced by radix descent over the order-preserving
+// keys: at each digit level a histogram of counts and of exp(s - max) sums
+// finds the digit where the mass accumulated from the top reaches the
+// target; at the full key T the last few keys equal to T are counted
+// arithmetically.  Every pass streams the row (L2-resident after the
+// selection layer wrote it).
+constexpr int kCovThreads = 1024;
+constexpr int kCovWarps = kCovThreads / 32;
+
+struct CovSmem {
+    unsigned cnt[kBins1];
+    float mass[kBins1];
+    float red[kCovWarps];
+    float fres[2];      // mass above the chosen digit, mass of the chosen digit
+    unsigned ures[3];   // digit, count above it, count of it
+};
+
+__device__ float cov_block_max(CovSmem &sm, float v)
+{
+    for (int off = 16; off >= 1; off >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(kFull, v, off));
+    if ((threadIdx.x & 31) == 0)
+        sm.red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float w = sm.red[threadIdx.x];
+        for (int off = 16; off >= 1; off >>= 1)
+            w = fmaxf(w, __shfl_xor_sync(kFull, w, off));
+        if (threadIdx.x == 0)
+            sm.fres[0] = w;
+    }
+    __syncthreads();
+    const float r = sm.fres[0];
+    __syncthreads();
+    return r;
+}
+
+// One warp: over bins nb-1 .. 0 (from the top), the first non-empty bin at
+// which the mass accumulated from the top reaches `target` (clamped to the
+// total, so rounding cannot leave it unreached; failing that, the lowest
+// non-empty bin).  Writes the digit, the count and mass above it, and its own
+// count and mass to ures / fres.
+__device__ void cov_find_digit(CovSmem &sm, int nb, float target)
+{
+    const int lane = threadIdx.x & 31;
+    const int per = nb / 32;  // bins per lane; lane 0 owns the top ones
+    float ms = 0.0f;
+    unsigned cs = 0;
+    for (int i = 0; i < per; ++i) {
+        const int bin = nb - 1 - lane * per - i;
+        ms += sm.mass[bin];
+        cs += sm.cnt[bin];
+    }
+    float mi = ms;
+    unsigned ci = cs;
+    for (int off = 1; off < 32; off <<= 1) {
+        const float mt = __shfl_up_sync(kFull, mi, off);
+        const unsigned ct = __shfl_up_sync(kFull, ci, off);
+        if (lane >= off) {
+            mi += mt;
+            ci += ct;
+        }
+    }
+    const float t = fminf(target, __shfl_sync(kFull, mi, 31));
+    const unsigned reach = __ballot_sync(kFull, cs > 0 && mi >= t);
+    const int src = reach ? __ffs(reach) - 1 : 31 - __clz(__ballot_sync(kFull, cs > 0));
+    if (lane == src) {
+        float run = mi - ms, prun = run;
+        unsigned crun = ci - cs, pcrun = crun;
+        int pick = nb - 1 - lane * per;
+        for (int i = 0; i < per; ++i) {
+            const int bin = nb - 1 - lane * per - i;
+            if (sm.cnt[bin] == 0)
+                continue;
+            pick = bin;
+            prun = run;
+            pcrun = crun;
+            if (run + sm.mass[bin] >= t)
+                break;
+            run += sm.mass[bin];
+            crun += sm.cnt[bin];
+        }
+        sm.ures[0] = (unsigned)pick;
+        sm.ures[1] = pcrun;
+        sm.ures[2] = sm.cnt[pick];
+        sm.fres[0] = prun;
+        sm.fres[1] = sm.mass[pick];
+    }
+}
+
+__global__ void __launch_bounds__(kCovThreads)
+coverage_kernel(const CoverageArgs a)
+{
+    __shared__ CovSmem sm;
+    const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const size_t bg = (size_t)b * a.Hkv + g;
+    int n = a.seq_lens[b];
+    n = n < 0 ? 0 : (n > a.Nmax ? a.Nmax : n);
+    const float *s = a.scores + bg * (size_t)a.Nmax;
+    pdl_wait();
+    pdl_launch_dependents();
+    if (n == 0) {
+        if (tid == 0)
+            a.row_k[bg] = 0;
+        return;
+    }
+    float mx = -INFINITY;
+    for (int i = tid; i < n; i += kCovThreads)
+        mx = fmaxf(mx, __ldcg(s + i));
+    const float M = cov_block_max(sm, mx);
+
+    uint32_t prefix = 0u, mask = 0u;
+    unsigned count_above = 0;
+    float mass_above = 0.0f, target = 0.0f;
+    // digit widths from the top: 11, 8, 8, 5 bits
+    for (int level = 0, top = 31; level < 4; ++level) {
+        const int width = level == 0 ? kBits1 : (level == 3 ? 5 : 8);
+        const int shift = top + 1 - width;
+        const unsigned nb = 1u << width;
+        for (int i = tid; i < (int)nb; i += kCovThreads) {
+            sm.cnt[i] = 0u;
+            sm.mass[i] = 0.0f;
+        }
+        __syncthreads();
+        for (int i = tid; i < n; i += kCovThreads) {
+            const float v = __ldcg(s + i);
+            const uint32_t key = order_key(v);
+            if ((key & mask) == prefix) {
+                const unsigned d = (key >> shift) & (nb - 1u);
+                atomicAdd(&sm.cnt[d], 1u);
+                atomicAdd(&sm.mass[d], expf(v - M));
+            }
+        }
+        __syncthreads();
+        if (level == 0) {
+            // the whole row's mass: the softmax denominator
+            float part = 0.0f;
+            for (int i = tid; i < (int)nb; i += kCovThreads)
+                part += sm.mass[i];
+            for (int off = 16; off >= 1; off >>= 1)
+                part += __shfl_xor_sync(kFull, part, off);
+            if ((tid & 31) == 0)
+                sm.red[tid >> 5] = part;
+            __syncthreads();
+            if (tid == 0) {
+                float L = 0.0f;
+                for (int w = 0; w < kCovWarps; ++w)
+                    L += sm.red[w];
+                sm.fres[0] = L;
+            }
+            __syncthreads();
+            target = (1.0f - a.tau) * sm.fres[0];
+            __syncthreads();
+        }
+        if (tid < 32)
+            cov_find_digit(sm, (int)nb, target - mass_above);
+        __syncthreads();
+        const unsigned d = sm.ures[0];
+        count_above += sm.ures[1];
+        mass_above += sm.fres[0];
+        const unsigned cnt_d = sm.ures[2];
+        const float mass_d = sm.fres[1];
+        prefix |= d << shift;
+        mask |= (nb - 1u) << shift;
+        top -= width;
+        __syncthreads();
+        if (level == 3 || cnt_d == 1u) {
+            // every key left equals the chosen one (or there is one): each carries
+            // mass_d / cnt_d; take as many as the remaining target needs
+            const float each = mass_d / (float)cnt_d;
+            const float need = target - mass_above;
+            unsigned j = cnt_d;
+            if (each > 0.0f && need <= each * (float)cnt_d) {
+                const float q = ceilf(need / each);
+                j = q < 1.0f ? 1u : (q > (float)cnt_d ? cnt_d : (unsigned)q);
+            }
+            if (tid == 0) {
+                const unsigned kc = count_above + j;
+                a.row_k[bg] = (int)(kc < (unsigned)a.kcap ? kc : (unsigned)a.kcap);
+            }
+            return;
+        }
+    }
 }
 
 template <int NT>
@@ -680,6 +882,20 @@ cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, bool pdl,
     }
     return threads == 512 ? launch_topk_nt<512>(a, batch, pdl, stream)
                           : launch_topk_nt<1024>(a, batch, pdl, stream);
+}
+
+cudaError_t launch_coverage(const CoverageArgs &a, int batch, bool pdl, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)batch);
+    cfg.blockDim = dim3(kCovThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, coverage_kernel, a);
 }
 
 }  // namespace td

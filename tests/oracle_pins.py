@@ -403,4 +403,30 @@ def pin_overlap_of_planted_selections(orc):
     assert orc.index_overlap(orc.topk(s1, k), orc.topk(s2, k)) == m
 
 
+def pin_coverage_closed_forms(orc):
+    """Coverage budgets with closed forms: uniform scores need ceil((1 - tau) n)
+    tokens; scores -i ln 2 give masses 2^-i / (2 - 2^(1-n)), so the budget is
+    the smallest k with (1 - 2^-k) >= (1 - tau)(1 - 2^-n), in any position
+    order; k_max caps it."""
+    assert orc.coverage_count(np.zeros(10), 0.25, 100) == 8          # 7.5 -> 8
+    assert orc.coverage_count(np.zeros(10), 0.25, 5) == 5            # capped
+    assert orc.coverage_count(np.full(1000, 3.5), 0.1, 1000) == 900
+    n = 20
+    geo = -np.arange(n) * math.log(2.0)
+    for tau in (0.5, 0.1, 0.01, 0.001):
+        want = next(k for k in range(1, n + 1)
+                    if 1.0 - 2.0 ** -k >= (1.0 - tau) * (1.0 - 2.0 ** -n))
+        assert orc.coverage_count(geo, tau, n) == want
+        perm = np.random.RandomState(int(tau * 1e4)).permutation(n)
+        assert orc.coverage_count(geo[perm], tau, n) == want
+    # one dominant score: p0 = e^10 / (e^10 + 4), the others e^0 / (e^10 + 4)
+    z = math.exp(10.0) + 4.0
+    s = np.array([10.0, 0.0, 0.0, 0.0, 0.0])
+    assert orc.coverage_count(s, 0.01, 5) == 1
+    tau = 1e-4
+    want = next(k for k in range(1, 6) if (math.exp(10.0) + (k - 1)) / z >= 1.0 - tau)
+    assert orc.coverage_count(s, tau, 5) == want == 3
+    assert orc.coverage_count(np.zeros(0), 0.1, 4) == 0
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -10,7 +10,7 @@ import pytest
 import oracle
 from oracle_pins import ALL_PINS
 
-MUTANTS = [1, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13]
+MUTANTS = [1, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)

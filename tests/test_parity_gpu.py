@@ -450,3 +450,50 @@ def test_index_overlap_of_consecutive_selection_layers(orc):
     assert counts.cpu().numpy().reshape(-1).tolist() == [orc.index_overlap(a[r], b[r])
                                                         for r in range(len(a))]
     assert 0 <= counts.min().item() and counts.max().item() <= wl.top_k
+
+
+def _coverage_ok(orc, s_ref, tau, k_max, k_got):
+    """k_got is the oracle's budget, or one off where the cumulative mass at the
+    cut is within fp32 rounding of 1 - tau (the kernel sums masses in fp32)."""
+    k_ref = orc.coverage_count(s_ref, tau, k_max)
+    if k_got == k_ref:
+        return True
+    if abs(k_got - k_ref) != 1:
+        return False
+    p = np.exp(s_ref - s_ref.max())
+    p /= p.sum()
+    order = np.lexsort((np.arange(len(s_ref)), -s_ref))
+    cut = np.cumsum(p[order])[min(k_got, k_ref) - 1]
+    return abs(cut - (1.0 - tau)) <= 1e-5
+
+
+@pytest.mark.parametrize("G,tau,k_max", [(1, 0.1, 2000), (1, 0.5, 64), (4, 0.01, 3000),
+                                          (2, 0.3, 1000), (8, 0.05, 500)])
+def test_coverage_selection(orc, G, tau, k_max):
+    Hkv, B, N = 2, 3, 3000
+    lens = [3000, 1777, 40]
+    shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
+    q, K, V, _ = W.random_case(60 + G, B, G * Hkv, Hkv, N, lens)
+    q = (q.float() * 3.0).to(torch.bfloat16)      # peakier attention: budgets well below N
+    qd, Kd, Vd = _dev(q, K, V)
+    seq = torch.as_tensor(np.asarray(lens, np.int32)).cuda()
+    idx = torch.full((B, Hkv, k_max), -7, dtype=torch.int32, device="cuda")
+    counts = torch.full((B, Hkv), -7, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(qd)
+    out32 = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
+    ws = td.Workspace(shape, k_max)
+    td.td_full_attn_select_coverage(shape, qd, Kd, Vd, seq, tau, k_max, idx, counts, out, out32,
+                                    None, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    check_outputs(out, out32, oracle_full(orc, shape, q, K, V, lens), "coverage layer outputs")
+    qb, Kb = W.u16(q), W.u16(K)
+    idx, counts = idx.cpu().numpy(), counts.cpu().numpy()
+    for b in range(B):
+        for g in range(Hkv):
+            s_ref = orc.group_scores(qb[b, g * G:(g + 1) * G], Kb[b, g], lens[b], shape.scale)
+            k_got = int(counts[b, g])
+            assert _coverage_ok(orc, s_ref, tau, k_max, k_got), f"b{b} g{g}: k={k_got}"
+            assert np.all(idx[b, g, k_got:] == -1)
+            ref_idx = orc.topk(s_ref, k_got)
+            check_index_set(idx[b, g, :k_got], ref_idx, s_ref, k_got, f"b{b} g{g}")
