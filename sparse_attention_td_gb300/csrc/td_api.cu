@@ -312,6 +312,7 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v, Ap
         if (cov.tau >= 0.0f) {
             td::CoverageArgs ca{};
             ca.scores = a.scores;
+            ca.hist = a.hist;
             ca.seq_lens = seq_lens;
             ca.row_k = (int32_t *)(c.wsb + c.ws.row_k);
             ca.Hkv = c.shape.num_kv_heads;

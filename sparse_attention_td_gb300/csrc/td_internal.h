@@ -70,6 +70,7 @@ struct TopkArgs {
 // whose top-k scores hold >= 1 - tau of softmax(scores) over the row).
 struct CoverageArgs {
     const float *scores;     // [B][Hkv][Nmax]
+    const unsigned *hist;    // [B*Hkv][kSelectBins] first-digit counts of the scores, or null
     const int32_t *seq_lens; // [B]
     int32_t *row_k;          // [B*Hkv] out
     int Hkv, Nmax, kcap;

@@ -651,13 +651,25 @@ topk_kernel(const TopkArgs a)
 constexpr int kCovThreads = 1024;
 constexpr int kCovWarps = kCovThreads / 32;
 
+constexpr int kCovCand = 3072;  // (key, mass) pairs of the crossing bin kept in shared memory
+constexpr int kCovBatch = 8;    // scores loaded per thread before they are used
+
 struct CovSmem {
     unsigned cnt[kBins1];
     float mass[kBins1];
     float red[kCovWarps];
     float fres[2];      // mass above the chosen digit, mass of the chosen digit
     unsigned ures[3];   // digit, count above it, count of it
+    unsigned ccount;
+    uint32_t ckey[kCovCand];
+    float cmass[kCovCand];
 };
+
+// Inverse of order_key.
+__device__ __forceinline__ float key_to_float(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
 
 __device__ float cov_block_max(CovSmem &sm, float v)
 {
@@ -748,10 +760,87 @@ coverage_kernel(const CoverageArgs a)
             a.row_k[bg] = 0;
         return;
     }
-    float mx = -INFINITY;
-    for (int i = tid; i < n; i += kCovThreads)
-        mx = fmaxf(mx, __ldcg(s + i));
-    const float M = cov_block_max(sm, mx);
+    // Reference for exp(s - M): any M >= max(s) keeps every term <= 1 and the
+    // mass ratios exact.  The selection layer's first-digit histogram gives
+    // one for free: the largest score of its highest non-empty bin.
+    float M;
+    if (a.hist) {
+        const unsigned *gh = a.hist + bg * kBins1;
+        int top_bin = -1;
+        for (int i = tid; i < kBins1; i += kCovThreads)
+            if (__ldcg(gh + i))
+                top_bin = i;
+        top_bin = __reduce_max_sync(kFull, top_bin);
+        if ((tid & 31) == 0)
+            sm.red[tid >> 5] = __int_as_float(top_bin);
+        __syncthreads();
+        int tb = -1;
+        for (int w = 0; w < kCovWarps; ++w)
+            tb = max(tb, __float_as_int(sm.red[w]));
+        const uint32_t kmin = (uint32_t)(tb < 0 ? 0 : tb) << (32 - kBits1);
+        M = key_to_float(kmin | (~0u >> kBits1));
+        // a bin this wide (huge scores) or not finite: take the exact maximum
+        if (!(isfinite(M) && M - key_to_float(kmin) <= 60.0f))
+            M = NAN;
+        __syncthreads();
+    }
+    if (!a.hist || isnan(M)) {
+        float mx = -INFINITY;
+        for (int i = tid; i < n; i += kCovThreads)
+            mx = fmaxf(mx, __ldcg(s + i));
+        M = cov_block_max(sm, mx);
+    }
+
+    // Levels after the first run on the crossing bin's elements, gathered into
+    // shared memory when they fit, else streamed from the row again.  The
+    // loops run in whole warps (f gets a validity flag) so that f can combine
+    // lanes with warp collectives.
+    bool gathered = false;
+    auto for_each = [&](uint32_t mask, uint32_t prefix, auto f) {
+        if (gathered) {
+            const unsigned cnt = sm.ccount;
+            for (unsigned base = 0; base < cnt; base += kCovThreads) {
+                const unsigned i = base + tid;
+                const bool in = i < cnt && (sm.ckey[i] & mask) == prefix;
+                f(in, in ? sm.ckey[i] : 0u, in ? sm.cmass[i] : 0.0f);
+            }
+        } else {
+            // kCovBatch loads in flight per thread before any is used
+            for (int base = 0; base < n; base += kCovThreads * kCovBatch) {
+                float v[kCovBatch];
+#pragma unroll
+                for (int j = 0; j < kCovBatch; ++j) {
+                    const int i = base + j * kCovThreads + tid;
+                    v[j] = i < n ? __ldcg(s + i) : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < kCovBatch; ++j) {
+                    const int i = base + j * kCovThreads + tid;
+                    const uint32_t key = order_key(v[j]);
+                    const bool in = i < n && (key & mask) == prefix;
+                    f(in, key, in ? expf(v[j] - M) : 0.0f);
+                }
+            }
+        }
+    };
+    // Histogram update with the lanes of a warp that hit the same bin
+    // combined first: scores crowd into few bins, and one shared-memory atomic
+    // per bin and warp instead of one per score removes most of the contention.
+    const int lane = tid & 31;
+    auto hist_add = [&](bool in, unsigned d, float e) {
+        const unsigned grp = __match_any_sync(kFull, in ? d : 0xffffffffu);
+        float sum = 0.0f;
+#pragma unroll
+        for (int src = 0; src < 32; ++src) {
+            const float ev = __shfl_sync(kFull, e, src);
+            if ((grp >> src) & 1u)
+                sum += ev;
+        }
+        if (in && __ffs(grp) - 1 == lane) {
+            atomicAdd(&sm.cnt[d], (unsigned)__popc(grp));
+            atomicAdd(&sm.mass[d], sum);
+        }
+    };
 
     uint32_t prefix = 0u, mask = 0u;
     unsigned count_above = 0;
@@ -766,18 +855,12 @@ coverage_kernel(const CoverageArgs a)
             sm.mass[i] = 0.0f;
         }
         __syncthreads();
-        for (int i = tid; i < n; i += kCovThreads) {
-            const float v = __ldcg(s + i);
-            const uint32_t key = order_key(v);
-            if ((key & mask) == prefix) {
-                const unsigned d = (key >> shift) & (nb - 1u);
-                atomicAdd(&sm.cnt[d], 1u);
-                atomicAdd(&sm.mass[d], expf(v - M));
-            }
-        }
+        for_each(mask, prefix, [&](bool in, uint32_t key, float e) {
+            hist_add(in, (key >> shift) & (nb - 1u), e);
+        });
         __syncthreads();
         if (level == 0) {
-            // the whole row's mass: the softmax denominator
+            // the whole row's mass: the softmax denominator (relative to M)
             float part = 0.0f;
             for (int i = tid; i < (int)nb; i += kCovThreads)
                 part += sm.mass[i];
@@ -823,6 +906,37 @@ coverage_kernel(const CoverageArgs a)
                 a.row_k[bg] = (int)(kc < (unsigned)a.kcap ? kc : (unsigned)a.kcap);
             }
             return;
+        }
+        if (level == 0 && cnt_d <= (unsigned)kCovCand) {
+            // one more read of the row: the crossing bin's (key, mass) pairs
+            if (tid == 0)
+                sm.ccount = 0u;
+            __syncthreads();
+            for (int base = 0; base < n; base += kCovThreads * kCovBatch) {
+                float v[kCovBatch];
+#pragma unroll
+                for (int j = 0; j < kCovBatch; ++j) {
+                    const int i = base + j * kCovThreads + tid;
+                    v[j] = i < n ? __ldcg(s + i) : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < kCovBatch; ++j) {
+                    const int i = base + j * kCovThreads + tid;
+                    const uint32_t key = order_key(v[j]);
+                    if (i < n && (key & mask) == prefix) {
+                        const unsigned slot = atomicAdd(&sm.ccount, 1u);
+                        if (slot < (unsigned)kCovCand) {  // exactly cnt_d land; the bound guards memory
+                            sm.ckey[slot] = key;
+                            sm.cmass[slot] = expf(v[j] - M);
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+            if (sm.ccount > (unsigned)kCovCand)
+                sm.ccount = kCovCand;  // unreachable: the histogram counted cnt_d of them
+            __syncthreads();
+            gathered = true;
         }
     }
 }
