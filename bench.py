@@ -295,13 +295,17 @@ def run_ours(args, world, rank, local):
     heavy = W.heavy_positions(wl)
     lens = W.seq_lens(wl)
     layers = [W.generate_layer(wl, layer, device, heavy[layer]) for layer in range(wl.layers)]
-    q = [x[0] for x in layers]
+    # every layer's q (and output) is a slice of one buffer, so a step's inputs
+    # and results cross PCIe in one copy each in the end-to-end pass
+    q_all = torch.stack([x[0] for x in layers])
+    q = list(q_all.unbind(0))
     K = [x[1] for x in layers]
     V = [x[2] for x in layers]
     seq = torch.as_tensor(lens).to(device)
     shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len,
                           scale=td.default_scale(wl.head_dim))
-    outs = [torch.empty_like(x) for x in q]
+    outs_all = torch.empty_like(q_all)
+    outs = list(outs_all.unbind(0))
     idx = torch.full((wl.batch, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device=device)
     ws = td.Workspace(shape, wl.top_k, device=device)
     modes = list(wl.modes)
@@ -402,16 +406,14 @@ def run_ours(args, world, rank, local):
     coverage = coverage_layer(td, torch, wl, shape, q, K, V, seq, ws, device, flush_l2, stream)
 
     # e2e: host q in (pinned), graph step, host outputs back, per step
-    q_host = [x.cpu().pin_memory() for x in q]
-    o_host = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
-    h2d = sum(x.numel() * x.element_size() for x in q_host)
-    d2h = sum(x.numel() * x.element_size() for x in o_host)
+    q_host = q_all.cpu().pin_memory()
+    o_host = torch.empty(outs_all.shape, dtype=outs_all.dtype).pin_memory()
+    h2d = q_host.numel() * q_host.element_size()
+    d2h = o_host.numel() * o_host.element_size()
     for _ in range(max(W_steps, 1)):
-        for src, dst in zip(q_host, q):
-            dst.copy_(src, non_blocking=True)
+        q_all.copy_(q_host, non_blocking=True)
         plan.launch(stream)
-        for src, dst in zip(outs, o_host):
-            dst.copy_(src, non_blocking=True)
+        o_host.copy_(outs_all, non_blocking=True)
     torch.cuda.synchronize(device)
     dist_barrier(world, device)
     e2e_ev = []
@@ -419,11 +421,9 @@ def run_ours(args, world, rank, local):
         flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for src, dst in zip(q_host, q):
-            dst.copy_(src, non_blocking=True)
+        q_all.copy_(q_host, non_blocking=True)
         plan.launch(stream)
-        for src, dst in zip(outs, o_host):
-            dst.copy_(src, non_blocking=True)
+        o_host.copy_(outs_all, non_blocking=True)
         b.record(stream)
         e2e_ev.append((a, b))
     torch.cuda.synchronize(device)
