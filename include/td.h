@@ -277,12 +277,12 @@ void td_plan_destroy(td_plan *plan);
  *
  * td_decode_step_append / td_plan_create_append: td_decode_step /
  * td_plan_create plus, per layer l, k_new[l] / v_new[l] (HOST arrays of
- * num_layers device pointers, both NULL for no append).  Each layer's
- * attention kernel writes its layer's new rows into the cache itself and
- * uses them for position p_b (full layers attend to it; a sparse layer uses
- * it when p_b is in the persisted set), so the step needs no extra launch.
- * The result equals td_kv_append on every layer followed by td_decode_step.
- * k_new/v_new may be written by the kernel just before the call.
+ * num_layers device pointers, both NULL for no append).  The step first
+ * writes every layer's new rows (one launch per 32 layers), then attends:
+ * full layers include position p_b, a sparse layer when p_b is in the
+ * persisted set.  The result equals td_kv_append on every layer followed by
+ * td_decode_step.  k_new/v_new may be written by the kernel just before the
+ * call.
  */
 td_status td_kv_append(const td_shape *shape, void *k_cache, void *v_cache, const void *k_new,
                        const void *v_new, const int32_t *seq_lens, void *stream);

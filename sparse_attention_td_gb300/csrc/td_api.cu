@@ -267,12 +267,6 @@ td_status check_layer_ptrs(const void *q, const void *k, const void *v, const vo
     return TD_OK;
 }
 
-// The new K/V rows of one layer (KV append), or none.
-struct Append {
-    const void *k_new = nullptr;
-    const void *v_new = nullptr;
-};
-
 // Launches of one full(+select) layer; arguments already validated.  pdl: the
 // attention kernel follows a kernel of the same call (programmatic dependent
 // launch); the first kernel of a call is ordered by the stream alone.
@@ -283,15 +277,13 @@ struct Coverage {
     int32_t *counts = nullptr;
 };
 
-td_status run_full(const Ctx &c, const void *q, const void *k, const void *v, Append ap,
+td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
                    const int32_t *seq_lens, int top_k, int32_t *idx_out, void *out,
                    float *out_f32, float *scores_out, cudaStream_t st, bool pdl,
                    Coverage cov = Coverage{})
 {
     const bool select = top_k > 0;
     td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
-    a.k_new = (const uint16_t *)ap.k_new;
-    a.v_new = (const uint16_t *)ap.v_new;
     a.scores = select ? (scores_out ? scores_out : (float *)(c.wsb + c.ws.scores)) : nullptr;
     a.hist = select ? (unsigned *)(c.wsb + c.ws.hist) : nullptr;
     plan_splits(c.shape, c.shape.max_seq_len, false, select, a.nsplit, a.chunk);
@@ -332,13 +324,11 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v, Ap
 
 // idx_dep: the kernel launched just before may have written `idx` (then the
 // sparse kernel waits for it before reading the set).
-td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v, Append ap,
+td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
                      const int32_t *seq_lens, const int32_t *idx, int top_k, void *out,
                      float *out_f32, cudaStream_t st, bool idx_dep, bool pdl)
 {
     td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
-    a.k_new = (const uint16_t *)ap.k_new;
-    a.v_new = (const uint16_t *)ap.v_new;
     a.idx = idx;
     a.top_k = top_k;
     a.idx_dep = idx_dep ? 1 : 0;
@@ -401,13 +391,23 @@ td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
                        const void *const *k_new, const void *const *v_new, cudaStream_t st,
                        void *const *layer_events)
 {
-    for (int l = 0; l < num_layers; ++l) {
-        Append ap;
-        if (k_new) {
-            ap.k_new = k_new[l];
-            ap.v_new = v_new[l];
+    // KV append first: one launch per kAppendLayers layers writes every layer's
+    // new rows; the first attention kernel is not overlapped with it.
+    for (int l0 = 0; k_new && l0 < num_layers; l0 += td::kAppendLayers) {
+        const int nl = num_layers - l0 < td::kAppendLayers ? num_layers - l0 : td::kAppendLayers;
+        td::AppendBatch batch{};
+        for (int j = 0; j < nl; ++j) {
+            batch.k[j] = (uint16_t *)k_caches[l0 + j];
+            batch.v[j] = (uint16_t *)v_caches[l0 + j];
+            batch.k_new[j] = (const uint16_t *)k_new[l0 + j];
+            batch.v_new[j] = (const uint16_t *)v_new[l0 + j];
         }
-        const bool pdl = l > 0;  // the first kernel waits for whatever precedes the call
+        if (td::launch_kv_append(batch, nl, seq_lens, c.shape.batch, c.shape.num_kv_heads,
+                                 c.shape.max_seq_len, st) != cudaSuccess)
+            return TD_ERR_CUDA;
+    }
+    for (int l = 0; l < num_layers; ++l) {
+        const bool pdl = l > 0;  // the first kernel waits for whatever precedes it
         if (layer_events && layer_events[l] &&
             cudaEventRecord((cudaEvent_t)layer_events[l], st) != cudaSuccess)
             return TD_ERR_CUDA;
@@ -415,15 +415,15 @@ td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
         td_status r;
         switch (modes[l]) {
         case TD_MODE_FULL:
-            r = run_full(c, q[l], k_caches[l], v_caches[l], ap, seq_lens, 0, nullptr, outs[l], of,
+            r = run_full(c, q[l], k_caches[l], v_caches[l], seq_lens, 0, nullptr, outs[l], of,
                          nullptr, st, pdl);
             break;
         case TD_MODE_FULL_SELECT:
-            r = run_full(c, q[l], k_caches[l], v_caches[l], ap, seq_lens, top_k, idx_buf,
+            r = run_full(c, q[l], k_caches[l], v_caches[l], seq_lens, top_k, idx_buf,
                          outs[l], of, nullptr, st, pdl);
             break;
         default:
-            r = run_sparse(c, q[l], k_caches[l], v_caches[l], ap, seq_lens, idx_buf, top_k,
+            r = run_sparse(c, q[l], k_caches[l], v_caches[l], seq_lens, idx_buf, top_k,
                            outs[l], of, st, l == 0 || modes[l - 1] == TD_MODE_FULL_SELECT, pdl);
             break;
         }
@@ -507,7 +507,7 @@ td_status td_full_attn_select(const td_shape *shape, const void *q, const void *
         return TD_ERR_INVALID_ARG;
     if (scores_out && !aligned(scores_out, 4))
         return TD_ERR_INVALID_ARG;
-    return run_full(c, q, k_cache, v_cache, Append{}, seq_lens, top_k, idx_out, out, out_f32,
+    return run_full(c, q, k_cache, v_cache, seq_lens, top_k, idx_out, out, out_f32,
                     top_k > 0 ? scores_out : nullptr, (cudaStream_t)stream, false);
 }
 
@@ -531,7 +531,7 @@ td_status td_full_attn_select_coverage(const td_shape *shape, const void *q, con
     Coverage cov;
     cov.tau = tau;
     cov.counts = counts_out;
-    return run_full(c, q, k_cache, v_cache, Append{}, seq_lens, k_max, idx_out, out, out_f32,
+    return run_full(c, q, k_cache, v_cache, seq_lens, k_max, idx_out, out, out_f32,
                     scores_out, (cudaStream_t)stream, false, cov);
 }
 
@@ -590,7 +590,7 @@ td_status td_sparse_attn(const td_shape *shape, const void *q, const void *k_cac
         return st;
     if (top_k < 1 || !idx || !aligned(idx, 4) || !seq_lens || !aligned(seq_lens, 4))
         return TD_ERR_INVALID_ARG;
-    return run_sparse(c, q, k_cache, v_cache, Append{}, seq_lens, idx, top_k, out, out_f32,
+    return run_sparse(c, q, k_cache, v_cache, seq_lens, idx, top_k, out, out_f32,
                       (cudaStream_t)stream, true, false);
 }
 
@@ -636,10 +636,13 @@ td_status td_kv_append(const td_shape *shape, void *k_cache, void *v_cache, cons
         !aligned(v_cache, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !seq_lens ||
         !aligned(seq_lens, 4))
         return TD_ERR_INVALID_ARG;
-    if (td::launch_kv_append((uint16_t *)k_cache, (uint16_t *)v_cache, (const uint16_t *)k_new,
-                             (const uint16_t *)v_new, seq_lens, shape->batch,
-                             shape->num_kv_heads, shape->max_seq_len, (cudaStream_t)stream) !=
-        cudaSuccess)
+    td::AppendBatch batch{};
+    batch.k[0] = (uint16_t *)k_cache;
+    batch.v[0] = (uint16_t *)v_cache;
+    batch.k_new[0] = (const uint16_t *)k_new;
+    batch.v_new[0] = (const uint16_t *)v_new;
+    if (td::launch_kv_append(batch, 1, seq_lens, shape->batch, shape->num_kv_heads,
+                             shape->max_seq_len, (cudaStream_t)stream) != cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }

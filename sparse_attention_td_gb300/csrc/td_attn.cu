@@ -188,11 +188,10 @@ namespace cg = cooperative_groups;
 // cluster (grid x = cluster x = splits) and are merged through distributed
 // shared memory; otherwise through global partials and an arrival ticket.
 // STAGED: rows reach shared memory by bulk copies (see the file comment).
-// APPEND: the step's new K/V rows are written into the cache (KV append).
-template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED, bool APPEND>
-// Register budgets: 64 (MHA, 4 CTAs per SM; 85 and 3 CTAs with selection or append), 128 (G = 2, 4:
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
+// Register budgets: 64 (MHA, 4 CTAs per SM; 85 and 3 CTAs with selection), 128 (G = 2, 4:
 // 2 CTAs per SM), 255 (G = 8).
-__global__ void __launch_bounds__(kAttnThreads, G == 1 ? (SELECT || APPEND ? 3 : 4) : (G <= 4 ? 2 : 1))
+__global__ void __launch_bounds__(kAttnThreads, G == 1 ? (SELECT ? 3 : 4) : (G <= 4 ? 2 : 1))
 attention_kernel(const AttnArgs a)
 {
     constexpr int U = kTokPerHalf;
@@ -236,11 +235,6 @@ attention_kernel(const AttnArgs a)
     const size_t bg = (size_t)b * a.Hkv + g;
     const uint16_t *kbase = a.k + bg * (size_t)a.Nmax * kHeadDim + c * 8;
     const uint16_t *vbase = a.v + bg * (size_t)a.Nmax * kHeadDim + c * 8;
-    // KV append: this step's token sits at position n_b - 1; its K/V rows come
-    // from k_new / v_new (written by a previous kernel, so read only after
-    // pdl_wait) and are written into the cache by one CTA.  No CTA reads that
-    // cache row in this launch: every use of position `pos` takes the new rows.
-    const int pos = (APPEND && n_b > 0) ? n_b - 1 : -1;
 
     if constexpr (SELECT) {
         for (int i = tid; i < kSelectBins; i += kAttnThreads)
@@ -278,23 +272,8 @@ attention_kernel(const AttnArgs a)
             if (t < t1)
                 row = SPARSE ? sm_rows[t - t0] : t;
             ok[u] = row >= 0;
-            const bool ld = ok[u] && (!APPEND || row != pos);  // an appended row comes from fix_new
-            kr[u] = ld ? load_row16(kbase + (size_t)row * kHeadDim) : make_uint4(0u, 0u, 0u, 0u);
-            vr[u] = ld ? load_row16(vbase + (size_t)row * kHeadDim) : make_uint4(0u, 0u, 0u, 0u);
-        }
-    };
-    // After pdl_wait: the appended token's rows, wherever the round holds it.
-    auto fix_new = [&](int base, uint4 (&kr)[U], uint4 (&vr)[U]) {
-        if (!APPEND || pos < 0)
-            return;
-        const int tb = base + (warp * 2 + half) * U;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int t = tb + u;
-            if (t < t1 && (SPARSE ? sm_rows[t - t0] : t) == pos) {
-                kr[u] = *reinterpret_cast<const uint4 *>(a.k_new + bg * kHeadDim + c * 8);
-                vr[u] = *reinterpret_cast<const uint4 *>(a.v_new + bg * kHeadDim + c * 8);
-            }
+            kr[u] = ok[u] ? load_row16(kbase + (size_t)row * kHeadDim) : make_uint4(0u, 0u, 0u, 0u);
+            vr[u] = ok[u] ? load_row16(vbase + (size_t)row * kHeadDim) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
     // Staged: stage `it` of the ring receives the 64 tokens starting at
@@ -333,7 +312,7 @@ attention_kernel(const AttnArgs a)
             for (int u = 0; u < U; ++u) {
                 const int t = tb + u;
                 const int row = t < t1 ? sm_rows[t - t0] : -1;
-                if (row >= 0 && row != pos) {
+                if (row >= 0) {
                     cp_async16(kst + (slot0 + u) * kStageRowBytes + c * 16,
                                 krows + (size_t)row * kHeadDim + c * 8);
                     cp_async16(vst + (slot0 + u) * kStageRowBytes + c * 16,
@@ -344,10 +323,10 @@ attention_kernel(const AttnArgs a)
         cp_async_commit();
     };
 
-    // No kernel of the step writes a cache row another kernel reads (an
-    // appended row is read from k_new / v_new), so the first round
-    // (register-streamed) or the first S stages (staged) are requested before
-    // waiting for the previous kernel; q and the appended rows may come from it.
+    // No attention or top-k kernel writes the cache (a step's KV append runs
+    // before its first attention kernel, which is not overlapped with it), so
+    // the first round (register-streamed) or the first S stages (staged) are
+    // requested before waiting for the previous kernel; q may come from it.
     uint4 kr0[U], vr0[U];
     bool ok0[U];
     if constexpr (STAGED && SPARSE) {
@@ -367,13 +346,6 @@ attention_kernel(const AttnArgs a)
         load_round(t0, kr0, vr0, ok0);
     }
     pdl_wait();
-    if (APPEND && pos >= 0 && warp == 0 && (SPARSE ? split == 0 : (pos >= t0 && pos < t1))) {
-        // half 0 copies the K row, half 1 the V row (16 lanes x 16 bytes)
-        const uint16_t *src = (half == 0 ? a.k_new : a.v_new) + bg * kHeadDim + c * 8;
-        uint16_t *dst = const_cast<uint16_t *>(half == 0 ? a.k : a.v) +
-                        (bg * (size_t)a.Nmax + pos) * kHeadDim + c * 8;
-        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
-    }
 
     // This lane's 8 dims of the group's G queries, as 4 dim pairs.
     float2 q2[G][4];
@@ -521,7 +493,6 @@ attention_kernel(const AttnArgs a)
                 vr[u] = ok[u] ? lds128(vst + (slot0 + u) * kStageRowBytes + c * 16)
                               : make_uint4(0u, 0u, 0u, 0u);
             }
-            fix_new(base, kr, vr);
             round(base, kr, vr, ok);
             issue_rows_cp(it + S);  // refill the slot just consumed (its values are used above)
         }
@@ -548,7 +519,6 @@ attention_kernel(const AttnArgs a)
                 vr[u] = ok[u] ? lds128(vst + (slot0 + u) * kStageRowBytes + c * 16)
                               : make_uint4(0u, 0u, 0u, 0u);
             }
-            fix_new(base, kr, vr);
             round(base, kr, vr, ok);
             failed = __syncthreads_or(!landed);  // also: every warp is done with stage st
             if (failed)
@@ -569,15 +539,12 @@ attention_kernel(const AttnArgs a)
             return;
         }
     } else {
-        if (t0 < t1) {
-            fix_new(t0, kr0, vr0);
+        if (t0 < t1)
             round(t0, kr0, vr0, ok0);
-        }
         for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
             uint4 kr[U], vr[U];
             bool ok[U];
             load_round(base, kr, vr, ok);
-            fix_new(base, kr, vr);
             round(base, kr, vr, ok);
         }
     }
@@ -797,7 +764,7 @@ constexpr size_t dyn_smem_bytes()
 }
 
 // The dynamic shared-memory opt-in of the staged kernels, once per device.
-template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED, bool APPEND>
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
 cudaError_t configure_once()
 {
     if (!STAGED)
@@ -809,7 +776,7 @@ cudaError_t configure_once()
         return e;
     if (dev >= 0 && dev < 64 && configured[dev])
         return cudaSuccess;
-    e = cudaFuncSetAttribute(attention_kernel<G, SPARSE, SELECT, CLUSTER, STAGED, APPEND>,
+    e = cudaFuncSetAttribute(attention_kernel<G, SPARSE, SELECT, CLUSTER, STAGED>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)dyn_smem_bytes<G, STAGED>());
     if (e == cudaSuccess && dev >= 0 && dev < 64)
@@ -817,13 +784,13 @@ cudaError_t configure_once()
     return e;
 }
 
-template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED, bool APPEND>
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
 cudaError_t launch_one(const AttnArgs &a, int batch, bool pdl, cudaStream_t stream)
 {
-    auto kern = attention_kernel<G, SPARSE, SELECT, CLUSTER, STAGED, APPEND>;
+    auto kern = attention_kernel<G, SPARSE, SELECT, CLUSTER, STAGED>;
     if (g_carveout >= 0)
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, g_carveout);
-    cudaError_t e0 = configure_once<G, SPARSE, SELECT, CLUSTER, STAGED, APPEND>();
+    cudaError_t e0 = configure_once<G, SPARSE, SELECT, CLUSTER, STAGED>();
     if (e0 != cudaSuccess)
         return e0;
     cudaLaunchConfig_t cfg = {};
@@ -856,28 +823,24 @@ template <int G, bool SPARSE, bool SELECT, bool STAGED>
 int occupancy_one()
 {
     int n = 0;
-    if (configure_once<G, SPARSE, SELECT, false, STAGED, false>() != cudaSuccess)
+    if (configure_once<G, SPARSE, SELECT, false, STAGED>() != cudaSuccess)
         return 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, attention_kernel<G, SPARSE, SELECT, false, STAGED, false>, kAttnThreads,
+            &n, attention_kernel<G, SPARSE, SELECT, false, STAGED>, kAttnThreads,
             dyn_smem_bytes<G, STAGED>()) != cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
 }
 
-// The cluster merge is built for the register-streamed kernels without append.
+// The cluster merge is built for the register-streamed kernels.
 template <int G, bool SPARSE, bool SELECT>
 cudaError_t launch_mode(bool cluster, bool staged, const AttnArgs &a, int batch, bool pdl,
                         cudaStream_t st)
 {
-    const bool append = a.k_new != nullptr;
-    if (cluster && !append)
-        return launch_one<G, SPARSE, SELECT, true, false, false>(a, batch, pdl, st);
-    if (staged)
-        return append ? launch_one<G, SPARSE, SELECT, false, true, true>(a, batch, pdl, st)
-                      : launch_one<G, SPARSE, SELECT, false, true, false>(a, batch, pdl, st);
-    return append ? launch_one<G, SPARSE, SELECT, false, false, true>(a, batch, pdl, st)
-                  : launch_one<G, SPARSE, SELECT, false, false, false>(a, batch, pdl, st);
+    if (cluster)
+        return launch_one<G, SPARSE, SELECT, true, false>(a, batch, pdl, st);
+    return staged ? launch_one<G, SPARSE, SELECT, false, true>(a, batch, pdl, st)
+                  : launch_one<G, SPARSE, SELECT, false, false>(a, batch, pdl, st);
 }
 
 template <int G>

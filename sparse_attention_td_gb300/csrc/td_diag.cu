@@ -3,8 +3,7 @@
 //
 // KV append: a decode step appends the new token's K and V rows to the cache
 // before attending (the growing KV cache of the decode phase, TidalDecode
-// review §二).  The attention kernels can do it themselves (the *_append
-// entry points); this kernel is the stand-alone form.
+// review §二).  One launch writes the rows of up to 32 layers.
 //
 // Overlap of two top-k sets per (batch row, KV head): the quantity the
 // TidalDecode review's token-selection sensitivity analysis plots (§三,
@@ -62,18 +61,19 @@ overlap_kernel(const int32_t *a, const int32_t *b, int top_k, int32_t *counts)
         counts[row] = (int32_t)sm_count;
 }
 
-// One warp per (batch row, KV head): lanes 0-15 copy the K row, 16-31 the V row.
-__global__ void kv_append_kernel(uint16_t *k, uint16_t *v, const uint16_t *k_new,
-                                 const uint16_t *v_new, const int32_t *seq_lens, int Hkv, int Nmax)
+// One warp per (batch row, KV head, layer): lanes 0-15 copy the K row, 16-31
+// the V row.
+__global__ void kv_append_kernel(const AppendBatch layers, const int32_t *seq_lens, int Hkv,
+                                 int Nmax)
 {
-    const int g = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
+    const int g = blockIdx.x, b = blockIdx.y, l = blockIdx.z, lane = threadIdx.x;
     const int n = seq_lens[b];
     if (n < 1 || n > Nmax)
         return;  // nothing to append (or a length the attention kernels flag)
     const size_t bg = (size_t)b * Hkv + g;
     const int c = lane & 15;
-    const uint16_t *src = (lane < 16 ? k_new : v_new) + bg * 128 + c * 8;
-    uint16_t *dst = (lane < 16 ? k : v) + (bg * (size_t)Nmax + (n - 1)) * 128 + c * 8;
+    const uint16_t *src = (lane < 16 ? layers.k_new[l] : layers.v_new[l]) + bg * 128 + c * 8;
+    uint16_t *dst = (lane < 16 ? layers.k[l] : layers.v[l]) + (bg * (size_t)Nmax + (n - 1)) * 128 + c * 8;
     *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
 }
 
@@ -88,14 +88,15 @@ cudaError_t launch_index_overlap(const int32_t *a, const int32_t *b, int rows, i
     return cudaGetLastError();
 }
 
-cudaError_t launch_kv_append(uint16_t *k, uint16_t *v, const uint16_t *k_new,
-                             const uint16_t *v_new, const int32_t *seq_lens, int batch, int Hkv,
-                             int Nmax, cudaStream_t stream)
+cudaError_t launch_kv_append(const AppendBatch &layers, int num_layers, const int32_t *seq_lens,
+                             int batch, int Hkv, int Nmax, cudaStream_t stream)
 {
-    if (batch <= 0 || Hkv <= 0)
+    if (batch <= 0 || Hkv <= 0 || num_layers <= 0)
         return cudaSuccess;
-    kv_append_kernel<<<dim3((unsigned)Hkv, (unsigned)batch), 32, 0, stream>>>(k, v, k_new, v_new,
-                                                                           seq_lens, Hkv, Nmax);
+    if (num_layers > kAppendLayers)
+        return cudaErrorInvalidValue;
+    kv_append_kernel<<<dim3((unsigned)Hkv, (unsigned)batch, (unsigned)num_layers), 32, 0, stream>>>(
+        layers, seq_lens, Hkv, Nmax);
     return cudaGetLastError();
 }
 

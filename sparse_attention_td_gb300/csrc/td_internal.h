@@ -37,8 +37,6 @@ struct AttnArgs {
     const uint16_t *v;
     const int32_t *seq_lens; // [B]
     const int32_t *idx;      // sparse: [B][Hkv][top_k]
-    const uint16_t *k_new;   // KV append: [B][Hkv][128] rows of position seq_lens[b]-1, or null
-    const uint16_t *v_new;   //   (written into k / v by the kernel)
     uint16_t *out;           // [B][Hq][128]
     float *out_f32;          // optional
     float *scores;           // select: [B][Hkv][Nmax]
@@ -82,7 +80,6 @@ struct CoverageArgs {
 // a.nsplit <= kMaxClusterSplits); otherwise through global partials.
 // staged: K/V rows reach shared memory by bulk asynchronous copies into a
 // ring of stages (ignored when cluster is set); otherwise register-streamed.
-// a.k_new != null selects the KV-append kernels (never the cluster merge).
 // pdl: the launch may overlap the tail of the kernel before it on the stream
 // (programmatic dependent launch); only for a kernel whose predecessor is a
 // kernel of the same call.
@@ -94,10 +91,18 @@ cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, bool pdl,
                         cudaStream_t stream);
 cudaError_t launch_coverage(const CoverageArgs &a, int batch, bool pdl, cudaStream_t stream);
 
-// KV append: rows k_new/v_new [B][Hkv][128] written at position seq_lens[b]-1.
-cudaError_t launch_kv_append(uint16_t *k, uint16_t *v, const uint16_t *k_new,
-                             const uint16_t *v_new, const int32_t *seq_lens, int batch, int Hkv,
-                             int Nmax, cudaStream_t stream);
+// KV append of up to kAppendLayers layers in one launch: for each layer l,
+// rows k_new[l] / v_new[l] [B][Hkv][128] written at position seq_lens[b]-1 of
+// k[l] / v[l].
+constexpr int kAppendLayers = 32;
+struct AppendBatch {
+    uint16_t *k[kAppendLayers];
+    uint16_t *v[kAppendLayers];
+    const uint16_t *k_new[kAppendLayers];
+    const uint16_t *v_new[kAppendLayers];
+};
+cudaError_t launch_kv_append(const AppendBatch &layers, int num_layers, const int32_t *seq_lens,
+                             int batch, int Hkv, int Nmax, cudaStream_t stream);
 
 // counts[b*Hkv + g] = |a[b][g] ∩ b[b][g]| over two ascending, -1-padded index rows.
 cudaError_t launch_index_overlap(const int32_t *a, const int32_t *b, int rows, int top_k,
