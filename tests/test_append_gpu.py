@@ -88,7 +88,7 @@ def test_kv_append_writes_the_rows():
 
 @pytest.mark.parametrize("G", [1, 4])
 @pytest.mark.parametrize("schedule", ["figure2", "per_layer_select"])
-def test_fused_append_step_matches_oracle(orc, staged, G, schedule):
+def test_append_step_matches_oracle(orc, staged, G, schedule):
     Hkv, B, N, k = 2, 2, 3000, 64
     Hq = G * Hkv
     lens = [3000, 1234]
@@ -127,7 +127,7 @@ def test_fused_append_step_matches_oracle(orc, staged, G, schedule):
         check_outputs(outs[layer], outs32[layer], ref[layer], f"layer {layer}")
 
 
-def test_fused_append_equals_append_then_step():
+def test_step_append_equals_append_then_step():
     """td_decode_step_append == td_kv_append on every layer + td_decode_step,
     bit for bit (same kernels, same split plan), also as a replayed plan."""
     Hkv, G, B, N, k = 4, 2, 2, 5000, 128
@@ -137,17 +137,17 @@ def test_fused_append_equals_append_then_step():
     shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
     seq = torch.tensor(lens, dtype=torch.int32).cuda()
 
-    def run(fused, plan=False):
+    def run(in_step, plan=False):
         dev = [[t.cuda() for t in lay] for lay in layers]
         q, K, V, kn, vn = ([x[i] for x in dev] for i in range(5))
         outs = [torch.empty_like(x) for x in q]
         idx = torch.full((B, Hkv, k), -1, dtype=torch.int32, device="cuda")
         ws = td.Workspace(shape, k)
-        if fused and plan:
+        if in_step and plan:
             p = td.Plan(shape, modes, q, K, V, seq, k, idx, outs, None, ws, k_new=kn, v_new=vn)
             p.launch()
             p.launch()      # replaying rewrites the same rows: same result
-        elif fused:
+        elif in_step:
             td.td_decode_step(shape, modes, q, K, V, seq, k, idx, outs, None, ws, k_new=kn,
                               v_new=vn)
         else:
