@@ -891,6 +891,12 @@ coverage_kernel(const CoverageArgs a)
         mask |= (nb - 1u) << shift;
         top -= width;
         __syncthreads();
+        if (count_above >= (unsigned)a.kcap) {
+            // more keys above the cut than the row can hold: the budget is the cap
+            if (tid == 0)
+                a.row_k[bg] = a.kcap;
+            return;
+        }
         if (level == 3 || cnt_d == 1u) {
             // every key left equals the chosen one (or there is one): each carries
             // mass_d / cnt_d; take as many as the remaining target needs

@@ -198,3 +198,33 @@ def test_growing_context_over_steps(orc):
         assert np.array_equal(idx.cpu().numpy(), ref_idx)
         for layer in range(len(modes)):
             check_outputs(outs[layer], outs32[layer], ref[layer], f"n={n} layer {layer}")
+
+
+def test_append_over_more_layers_than_one_launch_takes(orc):
+    """40 layers: the step appends in two launches (32 + 8 layers); every
+    layer's cache gets its row and every layer attends to it."""
+    L, Hkv, G, B, N = 40, 2, 1, 2, 160
+    lens = [160, 77]
+    modes = [W.FULL] * L
+    layers = _case(21, B, G * Hkv, Hkv, N, lens, L, heavy_new=False)
+    shape = td.make_shape(B, G * Hkv, Hkv, N, scale=td.default_scale(D))
+    dev = [[t.cuda() for t in lay] for lay in layers]
+    q, K, V, kn, vn = ([x[i] for x in dev] for i in range(5))
+    outs = [torch.empty_like(x) for x in q]
+    outs32 = [torch.empty(x.shape, dtype=torch.float32, device="cuda") for x in q]
+    ws = td.Workspace(shape, 0)
+    td.td_decode_step(shape, modes, q, K, V, torch.tensor(lens, dtype=torch.int32).cuda(), 0, None,
+                      outs, outs32, ws, k_new=kn, v_new=vn)
+    torch.cuda.synchronize()
+    for layer in range(L):
+        Ka = _appended(layers[layer][1], layers[layer][3], lens)
+        Va = _appended(layers[layer][2], layers[layer][4], lens)
+        assert torch.equal(K[layer].cpu(), Ka) and torch.equal(V[layer].cpu(), Va), layer
+        if layer in (0, 31, 32, 39):
+            qb, Kb, Vb = W.u16(layers[layer][0]), W.u16(Ka), W.u16(Va)
+            ref = np.zeros((B, G * Hkv, D))
+            for b in range(B):
+                for h in range(G * Hkv):
+                    ref[b, h] = orc.attend(qb[b, h], Kb[b, h // G, :lens[b]], Vb[b, h // G, :lens[b]],
+                                           shape.scale)
+            check_outputs(outs[layer], outs32[layer], ref, f"layer {layer}")
