@@ -44,6 +44,7 @@ METRIC = ("decode-step attention latency (us) and achieved KV HBM GB/s vs peak, 
 DEFAULT_CONFIG = "llama2-7b-10k"
 FLUSH_BYTES = 1 << 30
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the roofline uses the measured copy peak)
 
 
 # ----------------------------------------------------------------- distributed
@@ -458,6 +459,7 @@ def run_ours(args, world, rank, local):
         rooflines[name] = {
             "kernel": kk["kernel"], "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
             "unit": "GB/s", "frac": round(ach / peak, 4),
+            "frac_of_nominal": round(ach / NOMINAL_HBM_GBS, 4),
             "traffic": measured_traffic(wl.name, name), "peak_source": f"{peak_kind} hbm_gbs",
             "algorithmic_bytes_per_launch": kk["bytes"], "launch_us": round(kk["launch_us"], 2),
             "share_of_traced_step": round(kk["share"], 4)}
