@@ -325,6 +325,7 @@ def run_ours(args, world, rank, local):
     plan_app = td.Plan(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws,
                        k_new=k_new, v_new=v_new)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    sink = torch.zeros(4096, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
     K_steps, W_steps = args.steps, args.warmup
 
@@ -375,12 +376,25 @@ def run_ours(args, world, rank, local):
         dist_barrier(world, device)
         # pass 2: per-layer events around each layer's launches
         traced = []
+        probe = []
         for _ in range(K_steps):
             flush_l2()
             e = [torch.cuda.Event(enable_timing=True) for _ in range(wl.layers + 1)]
             td.td_decode_step(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws,
                               stream=stream, layer_events=e)
             traced.append(e)
+        # pass 3: the same layers with only their K/V reads (the read probe), same
+        # launch shapes: the memory-system floor of each layer's access pattern
+        for _ in range(K_steps):
+            flush_l2()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(wl.layers + 1)]
+            for layer, m in enumerate(modes):
+                e[layer].record(stream)
+                td.td_probe_layer_reads(shape, K[layer], V[layer], seq,
+                                        idx if m == W.SPARSE else None, wl.top_k, sink,
+                                        stream=stream)
+            e[wl.layers].record(stream)
+            probe.append(e)
         torch.cuda.synchronize(device)
         dist_barrier(world, device)
     ppsa_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_ppsa) * 1e3
@@ -391,11 +405,14 @@ def run_ours(args, world, rank, local):
                           for e in traced])                      # [K, L] us
     traced_step_us = float(np.mean([e[0].elapsed_time(e[-1]) * 1e3 for e in traced]))
     layer_mean = per_layer.mean(axis=0)
-    by_mode = {}
+    probe_mean = np.array([[e[i].elapsed_time(e[i + 1]) * 1e3 for i in range(wl.layers)]
+                           for e in probe]).mean(axis=0)
+    by_mode, floor_by_mode = {}, {}
     for name, m in (("full", W.FULL), ("full_select", W.FULL_SELECT), ("sparse", W.SPARSE)):
         sel = [i for i, mm in enumerate(modes) if mm == m]
         if sel:
             by_mode[name] = float(np.mean(layer_mean[sel]))
+            floor_by_mode[name] = float(np.mean(probe_mean[sel]))
     ppsa_us = dist_max(ppsa_us, world, device)
     full_us = dist_max(full_us, world, device)
     sel_us = dist_max(sel_us, world, device)
@@ -447,11 +464,13 @@ def run_ours(args, world, rank, local):
     kernels["full"] = {
         "kernel": "attention_kernel<G,full> (split-K flash decode over all N_b tokens + combine)",
         "launch_us": full_launch_us, "bytes": bytes_model["per_launch"]["full"],
+        "floor_us": floor_by_mode.get("full", floor_by_mode.get("full_select")),
         "share": (full_launch_us * (counts["full"] + counts["full_select"])) / step_sum}
     if "sparse" in by_mode:
         kernels["sparse"] = {
             "kernel": "attention_kernel<G,sparse> (gather of the k persisted K/V rows + combine)",
             "launch_us": by_mode["sparse"], "bytes": bytes_model["per_launch"]["sparse"],
+            "floor_us": floor_by_mode["sparse"],
             "share": by_mode["sparse"] * counts["sparse"] / step_sum}
     rooflines = {}
     for name, kk in kernels.items():
@@ -462,6 +481,8 @@ def run_ours(args, world, rank, local):
             "frac_of_nominal": round(ach / NOMINAL_HBM_GBS, 4),
             "traffic": measured_traffic(wl.name, name), "peak_source": f"{peak_kind} hbm_gbs",
             "algorithmic_bytes_per_launch": kk["bytes"], "launch_us": round(kk["launch_us"], 2),
+            "read_floor_us": round(kk["floor_us"], 2),
+            "frac_of_read_floor": round(kk["floor_us"] / kk["launch_us"], 4),
             "share_of_traced_step": round(kk["share"], 4)}
     dominant = max(kernels, key=lambda k: kernels[k]["share"])
     sparse_gbs = rooflines["sparse"]["achieved"] if "sparse" in rooflines else None

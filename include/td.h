@@ -302,6 +302,21 @@ td_status td_plan_create_append(td_plan **plan, const td_shape *shape, int32_t n
                                 void *ws, size_t ws_bytes);
 
 /*
+ * Measurement aid (not part of the decode step): reads exactly the K/V rows
+ * one full layer (idx == NULL) or one sparse layer (idx = its index set)
+ * reads, with the same split plan, launch shape and 16-byte row loads as the
+ * register-streamed attention kernel, but no arithmetic beyond an XOR (which
+ * lands in sink[0..sink_words), device, caller-owned).  Timing it gives the
+ * memory-system floor of that layer's access pattern on the device.
+ * Invalid or padding index entries are skipped.  Errors: TD_ERR_INVALID_ARG
+ * for null or misaligned pointers, sink_words < 1 or (sparse) top_k outside
+ * [1, max_seq_len]; TD_ERR_CUDA if the launch fails.
+ */
+td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const void *v_cache,
+                               const int32_t *seq_lens, const int32_t *idx, int32_t top_k,
+                               uint32_t *sink, int32_t sink_words, void *stream);
+
+/*
  * Kernel tuning knobs (process-wide, not thread-safe; for sweeps):
  *   "full_ctas_per_sm", "sparse_ctas_per_sm": resident CTAs assumed per SM
  *   "full_waves", "sparse_waves": target waves of CTAs per launch

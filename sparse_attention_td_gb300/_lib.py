@@ -78,6 +78,8 @@ def lib():
     L.td_full_attn_select_coverage.restype = ctypes.c_int
     L.td_full_attn_select_coverage.argtypes = [shp, vp, vp, vp, vp, ctypes.c_float, i32, vp, vp,
                                                vp, vp, vp, vp, sz, vp]
+    L.td_probe_layer_reads.restype = ctypes.c_int
+    L.td_probe_layer_reads.argtypes = [shp, vp, vp, vp, vp, i32, vp, i32, vp]
     L.td_kv_append.restype = ctypes.c_int
     L.td_kv_append.argtypes = [shp, vp, vp, vp, vp, vp, vp]
     L.td_decode_step_append.restype = ctypes.c_int
@@ -311,6 +313,18 @@ class _StepArgs:
             n_new = nb * shape.num_kv_heads * shape.head_dim
             self.k_new = _ptr_array(k_new, "k_new", torch.bfloat16, n_new)
             self.v_new = _ptr_array(v_new, "v_new", torch.bfloat16, n_new)
+
+
+def td_probe_layer_reads(shape: Shape, k_cache, v_cache, seq_lens, idx, top_k, sink,
+                         stream=None):
+    """Measurement aid: the K/V reads of one full (idx None) or sparse layer only."""
+    nq, nkv, nb = _sizes(shape)
+    st = lib().td_probe_layer_reads(
+        ctypes.byref(shape), _dev(k_cache, "k_cache", torch.bfloat16, nkv),
+        _dev(v_cache, "v_cache", torch.bfloat16, nkv), _dev(seq_lens, "seq_lens", torch.int32, nb),
+        _dev(idx, "idx", torch.int32, nb * shape.num_kv_heads * max(int(top_k), 1), True),
+        int(top_k), _dev(sink, "sink", torch.int32, 1), int(sink.numel()), _stream(stream))
+    _check(st, "td_probe_layer_reads")
 
 
 def td_kv_append(shape: Shape, k_cache, v_cache, k_new, v_new, seq_lens, stream=None):

@@ -560,6 +560,34 @@ td_status td_topk_select(const td_shape *shape, const float *scores, const int32
     return TD_OK;
 }
 
+td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const void *v_cache,
+                               const int32_t *seq_lens, const int32_t *idx, int32_t top_k,
+                               uint32_t *sink, int32_t sink_words, void *stream)
+{
+    td_status st = check_shape(shape);
+    if (st)
+        return st;
+    const bool sparse = idx != nullptr;
+    if (!k_cache || !v_cache || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !seq_lens ||
+        !aligned(seq_lens, 4) || !sink || !aligned(sink, 4) || sink_words < 1 ||
+        (sparse && (!aligned(idx, 4) || top_k < 1 || top_k > shape->max_seq_len)))
+        return TD_ERR_INVALID_ARG;
+    td::ProbeArgs a{};
+    a.k = (const uint16_t *)k_cache;
+    a.v = (const uint16_t *)v_cache;
+    a.seq_lens = seq_lens;
+    a.idx = idx;
+    a.sink = sink;
+    a.sink_words = sink_words;
+    a.Hkv = shape->num_kv_heads;
+    a.Nmax = shape->max_seq_len;
+    a.top_k = sparse ? top_k : 0;
+    plan_splits(*shape, sparse ? top_k : shape->max_seq_len, sparse, false, a.nsplit, a.chunk);
+    if (td::launch_probe_reads(a, shape->batch, (cudaStream_t)stream) != cudaSuccess)
+        return TD_ERR_CUDA;
+    return TD_OK;
+}
+
 td_status td_index_overlap(const td_shape *shape, const int32_t *idx_a, const int32_t *idx_b,
                            int32_t top_k, int32_t *counts, void *stream)
 {

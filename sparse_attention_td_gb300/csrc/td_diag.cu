@@ -1,5 +1,5 @@
-// td_diag.cu -- small kernels around the decode step: KV append and the
-// overlap of index sets.
+// td_diag.cu -- small kernels around the decode step: KV append, the
+// overlap of index sets, and a read probe for measurement.
 //
 // KV append: a decode step appends the new token's K and V rows to the cache
 // before attending (the growing KV cache of the decode phase, TidalDecode
@@ -77,6 +77,73 @@ __global__ void kv_append_kernel(const AppendBatch layers, const int32_t *seq_le
     *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
 }
 
+// Measurement aid: the K/V reads of one attention launch and nothing else.
+// Same grid, split plan, index staging and 16-byte row loads (4 tokens of K
+// and V in flight per thread) as the register-streamed attention kernel; the
+// data only feed an XOR, one word of which each CTA stores.
+constexpr int kProbeThreads = 256;
+constexpr int kProbeTok = 4;
+
+__global__ void __launch_bounds__(kProbeThreads)
+probe_reads_kernel(const ProbeArgs a)
+{
+    __shared__ int sm_rows[kMaxSparseChunk];
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = lane >> 4, c = lane & 15;
+    int n_b = a.seq_lens[b];
+    n_b = n_b < 0 ? 0 : (n_b > a.Nmax ? a.Nmax : n_b);
+    const bool sparse = a.idx != nullptr;
+    const int n_total = sparse ? a.top_k : n_b;
+    const int t0 = split * a.chunk;
+    const int t1 = min(t0 + a.chunk, n_total);
+    if (t0 >= t1)
+        return;
+    const size_t bg = (size_t)b * a.Hkv + g;
+    const uint16_t *kb = a.k + bg * (size_t)a.Nmax * 128 + c * 8;
+    const uint16_t *vb = a.v + bg * (size_t)a.Nmax * 128 + c * 8;
+    if (sparse) {
+        const int32_t *ip = a.idx + bg * (size_t)a.top_k;
+        for (int j = tid; j < t1 - t0; j += kProbeThreads) {
+            const int r = ip[t0 + j];
+            sm_rows[j] = (r >= 0 && r < n_b) ? r : -1;
+        }
+        __syncthreads();
+    }
+    unsigned acc = 0;
+    for (int base = t0; base < t1; base += kProbeThreads / 16 * kProbeTok) {
+        const int tb = base + (warp * 2 + half) * kProbeTok;
+        uint4 kr[kProbeTok], vr[kProbeTok];
+#pragma unroll
+        for (int u = 0; u < kProbeTok; ++u) {
+            const int t = tb + u;
+            const int row = t < t1 ? (sparse ? sm_rows[t - t0] : t) : -1;
+            kr[u] = make_uint4(0u, 0u, 0u, 0u);
+            vr[u] = kr[u];
+            if (row >= 0) {
+                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(kr[u].x), "=r"(kr[u].y), "=r"(kr[u].z), "=r"(kr[u].w)
+                             : "l"(kb + (size_t)row * 128));
+                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(vr[u].x), "=r"(vr[u].y), "=r"(vr[u].z), "=r"(vr[u].w)
+                             : "l"(vb + (size_t)row * 128));
+            }
+        }
+        // every load of the round is issued before any of them is used
+#pragma unroll
+        for (int u = 0; u < kProbeTok; ++u)
+            asm volatile("" : "+r"(kr[u].x), "+r"(kr[u].y), "+r"(kr[u].z), "+r"(kr[u].w),
+                         "+r"(vr[u].x), "+r"(vr[u].y), "+r"(vr[u].z), "+r"(vr[u].w));
+#pragma unroll
+        for (int u = 0; u < kProbeTok; ++u)
+            acc ^= kr[u].x ^ kr[u].y ^ kr[u].z ^ kr[u].w ^ vr[u].x ^ vr[u].y ^ vr[u].z ^ vr[u].w;
+    }
+    for (int off = 16; off >= 1; off >>= 1)
+        acc ^= __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0)
+        atomicXor(a.sink + (bg * (size_t)gridDim.x + split) % a.sink_words, acc);
+}
+
 }  // namespace
 
 cudaError_t launch_index_overlap(const int32_t *a, const int32_t *b, int rows, int top_k,
@@ -97,6 +164,15 @@ cudaError_t launch_kv_append(const AppendBatch &layers, int num_layers, const in
         return cudaErrorInvalidValue;
     kv_append_kernel<<<dim3((unsigned)Hkv, (unsigned)batch, (unsigned)num_layers), 32, 0, stream>>>(
         layers, seq_lens, Hkv, Nmax);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_probe_reads(const ProbeArgs &a, int batch, cudaStream_t stream)
+{
+    if (batch <= 0 || a.Hkv <= 0 || a.nsplit <= 0)
+        return cudaSuccess;
+    probe_reads_kernel<<<dim3((unsigned)a.nsplit, (unsigned)a.Hkv, (unsigned)batch), kProbeThreads, 0,
+                         stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -108,6 +108,19 @@ cudaError_t launch_kv_append(const AppendBatch &layers, int num_layers, const in
 cudaError_t launch_index_overlap(const int32_t *a, const int32_t *b, int rows, int top_k,
                                  int32_t *counts, cudaStream_t stream);
 
+// Read probe (measurement aid): the K/V row reads of one attention launch
+// with the given split plan, folded into an XOR; idx == null reads the
+// contiguous rows of a full layer.
+struct ProbeArgs {
+    const uint16_t *k, *v;
+    const int32_t *seq_lens;
+    const int32_t *idx;      // sparse: [B][Hkv][top_k], or null for a full layer
+    uint32_t *sink;          // sink_words words
+    int sink_words;
+    int Hkv, Nmax, top_k, chunk, nsplit;
+};
+cudaError_t launch_probe_reads(const ProbeArgs &a, int batch, cudaStream_t stream);
+
 // Preferred shared-memory carveout (percent, -1 = driver default) for later attention launches.
 void set_attention_carveout(int percent);
 

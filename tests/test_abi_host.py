@@ -139,3 +139,12 @@ def test_index_overlap_rejects_bad_arguments(L):
     assert L.td_index_overlap(ctypes.byref(s), p, p, 0, p, None) == INVALID
     assert L.td_index_overlap(ctypes.byref(s), ctypes.c_void_p(258), p, 8, p, None) == INVALID
     assert L.td_index_overlap(ctypes.byref(shape(head_dim=64)), p, p, 8, p, None) == UNSUPPORTED
+
+
+def test_probe_rejects_bad_arguments(L):
+    s = shape()
+    p = ctypes.c_void_p(256)
+    assert L.td_probe_layer_reads(ctypes.byref(s), None, p, p, None, 0, p, 4, None) == INVALID
+    assert L.td_probe_layer_reads(ctypes.byref(s), p, p, p, None, 0, p, 0, None) == INVALID
+    assert L.td_probe_layer_reads(ctypes.byref(s), p, p, p, p, 0, p, 4, None) == INVALID     # k < 1
+    assert L.td_probe_layer_reads(ctypes.byref(s), p, p, p, p, 5000, p, 4, None) == INVALID  # k > N

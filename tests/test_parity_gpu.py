@@ -500,3 +500,33 @@ def test_coverage_selection(orc, G, tau, k_max, qscale):
             assert np.all(idx[b, g, k_got:] == -1)
             ref_idx = orc.topk(s_ref, k_got)
             check_index_set(idx[b, g, :k_got], ref_idx, s_ref, k_got, f"b{b} g{g}")
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_probe_reads_exactly_the_layer_rows(sparse):
+    """The read probe touches exactly the K/V rows its layer reads: the XOR of
+    everything it folds equals the XOR of those rows' words."""
+    G, Hkv, B, N, k = 2, 2, 3, 1500, 200
+    lens = [1500, 777, 50]
+    shape = td.make_shape(B, G * Hkv, Hkv, N)
+    _, K, V, _ = W.random_case(70, B, G * Hkv, Hkv, N, lens)
+    rs = np.random.RandomState(71)
+    idx = np.full((B, Hkv, k), -1, np.int32)
+    for b in range(B):
+        for g in range(Hkv):
+            m = min(k, lens[b])
+            idx[b, g, :m] = np.sort(rs.choice(lens[b], m, replace=False))
+    sink = torch.zeros(512, dtype=torch.int32, device="cuda")
+    td.td_probe_layer_reads(shape, K.cuda(), V.cuda(), torch.tensor(lens, dtype=torch.int32).cuda(),
+                            torch.as_tensor(idx).cuda() if sparse else None, k, sink)
+    torch.cuda.synchronize()
+    got = np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint32))
+    kw = W.u16(K).view(np.uint32).reshape(B, Hkv, N, 64)
+    vw = W.u16(V).view(np.uint32).reshape(B, Hkv, N, 64)
+    want = np.uint32(0)
+    for b in range(B):
+        for g in range(Hkv):
+            rows = idx[b, g][idx[b, g] >= 0] if sparse else np.arange(lens[b])
+            want ^= np.bitwise_xor.reduce(kw[b, g, rows].ravel(), initial=np.uint32(0))
+            want ^= np.bitwise_xor.reduce(vw[b, g, rows].ravel(), initial=np.uint32(0))
+    assert got == want
