@@ -99,7 +99,7 @@ long partial_slots(const td_shape &s, int top_k)
 }
 
 struct WsLayout {
-    size_t status, tickets, part_m, part_l, part_o, scores, hist, row_k, total;
+    size_t status, tickets, part_m, part_l, part_o, scores, hist, row_k, cov_cnt, cov_mass, total;
 };
 
 WsLayout ws_layout(const td_shape &s, int top_k)
@@ -128,6 +128,12 @@ WsLayout ws_layout(const td_shape &s, int top_k)
     w.row_k = off;  // per-row budgets of a coverage selection
     if (top_k > 0)
         off = align_up(off + units * sizeof(int32_t));
+    w.cov_cnt = off;  // first-digit count / mass histograms of a coverage selection (kept zero)
+    if (top_k > 0)
+        off = align_up(off + units * (size_t)td::kSelectBins * sizeof(unsigned));
+    w.cov_mass = off;
+    if (top_k > 0)
+        off = align_up(off + units * (size_t)td::kSelectBins * sizeof(float));
     w.total = off;
     return w;
 }
@@ -307,6 +313,8 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
             ca.hist = a.hist;
             ca.seq_lens = seq_lens;
             ca.row_k = (int32_t *)(c.wsb + c.ws.row_k);
+            ca.gcnt = (unsigned *)(c.wsb + c.ws.cov_cnt);
+            ca.gmass = (float *)(c.wsb + c.ws.cov_mass);
             ca.Hkv = c.shape.num_kv_heads;
             ca.Nmax = c.shape.max_seq_len;
             ca.kcap = top_k;

@@ -71,6 +71,8 @@ struct CoverageArgs {
     const unsigned *hist;    // [B*Hkv][kSelectBins] first-digit counts of the scores, or null
     const int32_t *seq_lens; // [B]
     int32_t *row_k;          // [B*Hkv] out
+    unsigned *gcnt;          // [B*Hkv][kSelectBins] first-digit counts (zero on entry), or null
+    float *gmass;            // [B*Hkv][kSelectBins] first-digit mass sums (zero on entry)
     int Hkv, Nmax, kcap;
     float tau;
 };

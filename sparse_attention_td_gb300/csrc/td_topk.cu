@@ -744,6 +744,89 @@ __device__ void cov_find_digit(CovSmem &sm, int nb, float target)
     }
 }
 
+// Reference for exp(s - M): any M >= max(s) keeps every term <= 1 and the
+// mass ratios exact.  The selection layer's first-digit histogram gives one
+// for free: the largest score of its highest non-empty bin.  NaN when that
+// bin is too wide (huge scores) or not finite: then the exact maximum is
+// needed.  Every thread of the block must call it (it uses `red`).
+template <int NT>
+__device__ float cov_reference(const unsigned *gh, float *red)
+{
+    constexpr int nw = NT / 32;
+    int top_bin = -1;
+    for (int i = threadIdx.x; i < kBins1; i += NT)
+        if (__ldcg(gh + i))
+            top_bin = i;
+    top_bin = __reduce_max_sync(kFull, top_bin);
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = __int_as_float(top_bin);
+    __syncthreads();
+    int tb = -1;
+    for (int w = 0; w < nw; ++w)
+        tb = max(tb, __float_as_int(red[w]));
+    __syncthreads();
+    const uint32_t kmin = (uint32_t)(tb < 0 ? 0 : tb) << (32 - kBits1);
+    const float M = key_to_float(kmin | (~0u >> kBits1));
+    return (isfinite(M) && M - key_to_float(kmin) <= 60.0f) ? M : NAN;
+}
+
+// First digit of the coverage descent, spread over several CTAs per row:
+// counts and exp(s - M) sums of the top 11 bits of this CTA's part of the
+// row, added into the row's global histogram.  Rows whose reference is not
+// usable are left to the single-CTA path.
+constexpr int kCovPartThreads = 256;
+constexpr int kCovPart = kCovPartThreads * 16;  // scores per CTA
+
+__global__ void __launch_bounds__(kCovPartThreads)
+coverage_part_kernel(const CoverageArgs a)
+{
+    __shared__ unsigned cnt[kBins1];
+    __shared__ float mass[kBins1];
+    __shared__ float red[kCovPartThreads / 32];
+    const int part = blockIdx.x, g = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    const size_t bg = (size_t)b * a.Hkv + g;
+    int n = a.seq_lens[b];
+    n = n < 0 ? 0 : (n > a.Nmax ? a.Nmax : n);
+    pdl_wait();
+    pdl_launch_dependents();
+    const int i0 = part * kCovPart;
+    if (i0 >= n)
+        return;
+    const float M = cov_reference<kCovPartThreads>(a.hist + bg * kBins1, red);
+    if (isnan(M))
+        return;
+    for (int i = tid; i < kBins1; i += kCovPartThreads) {
+        cnt[i] = 0u;
+        mass[i] = 0.0f;
+    }
+    __syncthreads();
+    const float *s = a.scores + bg * (size_t)a.Nmax;
+    const int i1 = min(i0 + kCovPart, n);
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int i = i0 + j * kCovPartThreads + tid;
+        v[j] = i < i1 ? __ldcg(s + i) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int i = i0 + j * kCovPartThreads + tid;
+        if (i < i1) {
+            const unsigned d = order_key(v[j]) >> (32 - kBits1);
+            atomicAdd(&cnt[d], 1u);
+            atomicAdd(&mass[d], expf(v[j] - M));
+        }
+    }
+    __syncthreads();
+    unsigned *gc = a.gcnt + bg * kBins1;
+    float *gm = a.gmass + bg * kBins1;
+    for (int i = tid; i < kBins1; i += kCovPartThreads)
+        if (cnt[i]) {
+            atomicAdd(&gc[i], cnt[i]);
+            atomicAdd(&gm[i], mass[i]);
+        }
+}
+
 __global__ void __launch_bounds__(kCovThreads)
 coverage_kernel(const CoverageArgs a)
 {
@@ -760,31 +843,11 @@ coverage_kernel(const CoverageArgs a)
             a.row_k[bg] = 0;
         return;
     }
-    // Reference for exp(s - M): any M >= max(s) keeps every term <= 1 and the
-    // mass ratios exact.  The selection layer's first-digit histogram gives
-    // one for free: the largest score of its highest non-empty bin.
-    float M;
-    if (a.hist) {
-        const unsigned *gh = a.hist + bg * kBins1;
-        int top_bin = -1;
-        for (int i = tid; i < kBins1; i += kCovThreads)
-            if (__ldcg(gh + i))
-                top_bin = i;
-        top_bin = __reduce_max_sync(kFull, top_bin);
-        if ((tid & 31) == 0)
-            sm.red[tid >> 5] = __int_as_float(top_bin);
-        __syncthreads();
-        int tb = -1;
-        for (int w = 0; w < kCovWarps; ++w)
-            tb = max(tb, __float_as_int(sm.red[w]));
-        const uint32_t kmin = (uint32_t)(tb < 0 ? 0 : tb) << (32 - kBits1);
-        M = key_to_float(kmin | (~0u >> kBits1));
-        // a bin this wide (huge scores) or not finite: take the exact maximum
-        if (!(isfinite(M) && M - key_to_float(kmin) <= 60.0f))
-            M = NAN;
-        __syncthreads();
-    }
-    if (!a.hist || isnan(M)) {
+    // the reference M the part kernels used (same histogram, same value), or
+    // the exact maximum where it is not usable
+    float M = a.hist ? cov_reference<kCovThreads>(a.hist + bg * kBins1, sm.red) : NAN;
+    const bool have_parts = a.gcnt && !isnan(M);
+    if (isnan(M)) {
         float mx = -INFINITY;
         for (int i = tid; i < n; i += kCovThreads)
             mx = fmaxf(mx, __ldcg(s + i));
@@ -850,14 +913,26 @@ coverage_kernel(const CoverageArgs a)
         const int width = level == 0 ? kBits1 : (level == 3 ? 5 : 8);
         const int shift = top + 1 - width;
         const unsigned nb = 1u << width;
-        for (int i = tid; i < (int)nb; i += kCovThreads) {
-            sm.cnt[i] = 0u;
-            sm.mass[i] = 0.0f;
+        if (level == 0 && have_parts) {
+            // the part kernels' first-digit histogram; cleared for the next use
+            unsigned *gc = a.gcnt + bg * kBins1;
+            float *gm = a.gmass + bg * kBins1;
+            for (int i = tid; i < (int)nb; i += kCovThreads) {
+                sm.cnt[i] = __ldcg(gc + i);
+                sm.mass[i] = __ldcg(gm + i);
+                gc[i] = 0u;
+                gm[i] = 0.0f;
+            }
+        } else {
+            for (int i = tid; i < (int)nb; i += kCovThreads) {
+                sm.cnt[i] = 0u;
+                sm.mass[i] = 0.0f;
+            }
+            __syncthreads();
+            for_each(mask, prefix, [&](bool in, uint32_t key, float e) {
+                hist_add(in, (key >> shift) & (nb - 1u), e);
+            });
         }
-        __syncthreads();
-        for_each(mask, prefix, [&](bool in, uint32_t key, float e) {
-            hist_add(in, (key >> shift) & (nb - 1u), e);
-        });
         __syncthreads();
         if (level == 0) {
             // the whole row's mass: the softmax denominator (relative to M)
@@ -1006,6 +1081,22 @@ cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, bool pdl,
 
 cudaError_t launch_coverage(const CoverageArgs &a, int batch, bool pdl, cudaStream_t stream)
 {
+    if (a.gcnt && a.hist) {
+        cudaLaunchConfig_t pc = {};
+        pc.gridDim = dim3((unsigned)((a.Nmax + kCovPart - 1) / kCovPart), (unsigned)a.Hkv,
+                          (unsigned)batch);
+        pc.blockDim = dim3(kCovPartThreads);
+        pc.stream = stream;
+        cudaLaunchAttribute pattr[1];
+        pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pattr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+        pc.attrs = pattr;
+        pc.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&pc, coverage_part_kernel, a);
+        if (e != cudaSuccess)
+            return e;
+        pdl = true;  // the row kernel follows the part kernel
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)batch);
     cfg.blockDim = dim3(kCovThreads);
