@@ -30,71 +30,11 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include "td_attn_common.cuh"
 #include "td_internal.h"
 
 namespace td {
 namespace {
-
-constexpr unsigned kFull = 0xffffffffu;
-constexpr float kLog2e = 1.4426950408889634f;
-
-// bf16 -> fp32 is exact: a bf16 value is the upper half of its fp32 word.
-// Pairs of consecutive dims as float2 (2j, 2j+1), for the packed fp32 pipe
-// (one fma.rn.f32x2 does two IEEE fmas).
-__device__ __forceinline__ void unpack8x2(const uint4 v, float2 (&f)[4])
-{
-    f[0] = make_float2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
-    f[1] = make_float2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-    f[2] = make_float2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
-    f[3] = make_float2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
-}
-
-// K/V rows are read exactly once per layer: read-only path, no L1 allocation.
-__device__ __forceinline__ uint4 load_row16(const uint16_t *p)
-{
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-// Programmatic dependent launch: the next kernel of the step may start while
-// this one finishes.  Before pdl_wait() a kernel touches only what no kernel
-// of the step writes (seq_lens, the K/V cache, and an index set produced
-// earlier than by the kernel right before); after it, everything the
-// previous kernel wrote (q in a full model, index set, scores, workspace) is
-// complete and visible.
-__device__ __forceinline__ void pdl_wait()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Order-preserving 32-bit key of a score (as in the top-k kernel): larger
-// float -> larger unsigned, -0.0 equal to +0.0.
-__device__ __forceinline__ uint32_t order_key(float f)
-{
-    uint32_t u = __float_as_uint(f);
-    if (u == 0x80000000u)
-        u = 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float safe_exp2_diff(float x, float m)
-{
-    // exp2(x - m) with m = -inf meaning "no token seen yet" (weight 0)
-    return (m == -CUDART_INF_F) ? 0.0f : exp2f(x - m);
-}
-
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f)
-{
-    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
 
 // ---- staged path: bulk copies into shared memory completing on mbarriers
 constexpr int kStageRowBytes = kHeadDim * 2;                   // one bf16 row
@@ -660,99 +600,7 @@ attention_kernel(const AttnArgs a)
         cluster.sync();  // keep every split's shared memory alive until split 0 has read it
         return;
     }
-    if (nsplit_b == 1) {
-        for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
-            const int h = e / kHeadDim, d = e % kHeadDim;
-            float acc = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w)
-                acc += sm_o[w][h][d] * sm_w[w][h];
-            const float L = sm_L[h];
-            const float val = L > 0.0f ? acc / L : 0.0f;
-            a.out[(out_row0 + h) * kHeadDim + d] = f32_to_bf16_rn(val);
-            if (a.out_f32)
-                a.out_f32[(out_row0 + h) * kHeadDim + d] = val;
-        }
-        return;
-    }
-
-    // Several splits: publish this split's partial result.
-    const size_t pbase = (bg * (size_t)a.nsplit + split) * G;
-    for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
-        const int h = e / kHeadDim, d = e % kHeadDim;
-        float acc = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w)
-            acc += sm_o[w][h][d] * sm_w[w][h];
-        a.part_o[(pbase + h) * kHeadDim + d] = acc;
-    }
-    if (tid < G) {
-        a.part_m[pbase + tid] = sm_M[tid];
-        a.part_l[pbase + tid] = sm_L[tid];
-    }
-    // One thread takes the ticket with a release-acquire atomic at GPU scope:
-    // the barrier orders the CTA's partial stores before it, and in the last
-    // CTA the acquire plus the next barrier order the merge's loads after
-    // every other split's release.  No thread-wide fences.
-    __syncthreads();
-    if (tid == 0) {
-        unsigned ticket;
-        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
-                     : "=r"(ticket)
-                     : "l"(a.tickets + bg)
-                     : "memory");
-        sm_last = (ticket == (unsigned)(nsplit_b - 1));
-    }
-    __syncthreads();
-    if (!sm_last)
-        return;
-
-    // Last CTA of this (batch, KV head): merge all splits.  Each output
-    // element's thread reads every split's (m, l) of its head and its own o
-    // values as one batch of independent loads (chunks of kMergeChunk splits),
-    // then reduces locally: one round trip instead of three with barriers.
-    const size_t pb0 = bg * (size_t)a.nsplit * G;
-    constexpr int kMergeChunk = 16;
-    for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
-        const int h = e / kHeadDim, d = e % kHeadDim;
-        float M = -CUDART_INF_F, L = 0.0f, acc = 0.0f;
-        for (int s0 = 0; s0 < nsplit_b; s0 += kMergeChunk) {
-            float mv[kMergeChunk], lv[kMergeChunk], ov[kMergeChunk];
-#pragma unroll
-            for (int j = 0; j < kMergeChunk; ++j) {
-                const int s = s0 + j;
-                mv[j] = -CUDART_INF_F;
-                lv[j] = 0.0f;
-                ov[j] = 0.0f;
-                if (s < nsplit_b) {
-                    const size_t ps = pb0 + (size_t)s * G + h;
-                    mv[j] = __ldcg(&a.part_m[ps]);
-                    lv[j] = __ldcg(&a.part_l[ps]);
-                    ov[j] = __ldcg(&a.part_o[ps * kHeadDim + d]);
-                }
-            }
-            float Mc = M;
-#pragma unroll
-            for (int j = 0; j < kMergeChunk; ++j)
-                Mc = fmaxf(Mc, mv[j]);
-            const float r = safe_exp2_diff(M, Mc);  // rescale what earlier chunks added
-            acc *= r;
-            L *= r;
-#pragma unroll
-            for (int j = 0; j < kMergeChunk; ++j) {
-                const float wt = safe_exp2_diff(mv[j], Mc);
-                acc += wt * ov[j];
-                L += wt * lv[j];
-            }
-            M = Mc;
-        }
-        const float val = L > 0.0f ? acc / L : 0.0f;
-        a.out[(out_row0 + h) * kHeadDim + d] = f32_to_bf16_rn(val);
-        if (a.out_f32)
-            a.out_f32[(out_row0 + h) * kHeadDim + d] = val;
-    }
-    if (tid == 0)
-        a.tickets[bg] = 0u;  // ready for the next launch on this workspace
+    finish_splits<G>(a, sm_o, sm_w, sm_M, sm_L, &sm_last, bg, split, nsplit_b, out_row0);
 }
 
 int g_carveout = -1;  // preferred shared-memory carveout (percent) for the attention kernels
