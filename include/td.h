@@ -333,6 +333,10 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *   "sparse_staged": 1 stages the gathered rows of sparse layers through a
  *                  per-thread cp.async ring in shared memory; 0 (default) or
  *                  negative streams them into registers
+ *   "mma": 1 (and the default) runs grouped-query layers with G = 4 or 8 on
+ *          the tensor cores (mma.sync over the group's heads); 0 on the CUDA
+ *          cores (where "full_staged" / "sparse_staged" apply); negative
+ *          restores the default
  *   "topk_threads": 1024 or 512 threads per top-k row; other values restore
  *                   the default (1024 when batch * kv_heads fits one wave of
  *                   one CTA per SM, else 512 with two CTAs per SM)

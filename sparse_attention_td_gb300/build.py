@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtd.so")
-SOURCES = ["td_api.cu", "td_attn.cu", "td_topk.cu", "td_noalloc.cu", "td_diag.cu"]
+SOURCES = ["td_api.cu", "td_attn.cu", "td_attn_mma.cu", "td_topk.cu", "td_noalloc.cu", "td_diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -34,12 +34,17 @@ struct Tuning {
                                  // (bulk copies); 0: register-streamed; -1: staged when G >= 4
     int sparse_staged = 0;       // 1: sparse kernels stage the gathered rows through shared memory
                                  // (per-thread cp.async ring); 0: register-streamed
+    int mma = -1;                // 1 / -1 (default): tensor-core kernels for G = 4, 8; 0: CUDA cores
 };
 Tuning g_tuning;
 const Tuning kDefaultTuning;
 
 // Measured on GB300: staging pays for the grouped-query full kernels (G >= 4,
 // issue-bound at two CTAs per SM) and for none of the others.
+// Measured on GB300: the tensor-core kernels take 6-9% off grouped-query
+// full layers and match the CUDA-core ones on sparse layers.
+bool mma_for(int G) { return g_tuning.mma != 0 && td::mma_supported(G); }
+
 bool staged_for(bool sparse, int G)
 {
     if (sparse)
@@ -187,7 +192,8 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
     const long units = (long)s.batch * s.num_kv_heads;
     int per_sm = sparse ? g_tuning.sparse_ctas_per_sm : g_tuning.full_ctas_per_sm;
     if (per_sm <= 0)
-        per_sm = td::attention_ctas_per_sm(G, sparse, select, staged_for(sparse, G));
+        per_sm = mma_for(G) ? td::attention_mma_ctas_per_sm(G, sparse, select)
+                            : td::attention_ctas_per_sm(G, sparse, select, staged_for(sparse, G));
     const long slots = (long)device_sm_count() * per_sm;  // resident CTAs per wave
     int waves = sparse ? g_tuning.sparse_waves : g_tuning.full_waves;
     if (waves <= 0)  // one wave of long CTAs when the pairs are few; more, shorter
@@ -294,8 +300,11 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
     a.hist = select ? (unsigned *)(c.wsb + c.ws.hist) : nullptr;
     plan_splits(c.shape, c.shape.max_seq_len, false, select, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
-    if (td::launch_attention(c.G, false, select, cluster, staged_for(false, c.G), a, c.shape.batch,
-                             pdl, st) != cudaSuccess)
+    const cudaError_t le =
+        mma_for(c.G) ? td::launch_attention_mma(c.G, false, select, a, c.shape.batch, pdl, st)
+                     : td::launch_attention(c.G, false, select, cluster, staged_for(false, c.G), a,
+                                            c.shape.batch, pdl, st);
+    if (le != cudaSuccess)
         return TD_ERR_CUDA;
     if (select) {
         td::TopkArgs t{};
@@ -342,8 +351,11 @@ td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
     a.idx_dep = idx_dep ? 1 : 0;
     plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
-    if (td::launch_attention(c.G, true, false, cluster, staged_for(true, c.G), a, c.shape.batch, pdl,
-                             st) != cudaSuccess)
+    const cudaError_t le =
+        mma_for(c.G) ? td::launch_attention_mma(c.G, true, false, a, c.shape.batch, pdl, st)
+                     : td::launch_attention(c.G, true, false, cluster, staged_for(true, c.G), a,
+                                            c.shape.batch, pdl, st);
+    if (le != cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }
@@ -787,6 +799,8 @@ td_status td_set_tuning(const char *key, int32_t value)
         g_tuning.full_staged = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.full_staged);  // <0: auto
     else if (!strcmp(key, "sparse_staged"))
         g_tuning.sparse_staged = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.sparse_staged);
+    else if (!strcmp(key, "mma"))
+        g_tuning.mma = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.mma);
     else if (!strcmp(key, "topk_threads"))
         g_tuning.topk_threads = (value == 512 || value == 1024) ? value : 0;
     else if (!strcmp(key, "attn_carveout"))

@@ -123,6 +123,14 @@ struct ProbeArgs {
 };
 cudaError_t launch_probe_reads(const ProbeArgs &a, int batch, cudaStream_t stream);
 
+// Tensor-core attention (mma.sync over a KV head's G query heads) for
+// G = 4 and 8: same arguments and results as launch_attention (no cluster
+// merge, register-fed fragments).
+bool mma_supported(int G);
+cudaError_t launch_attention_mma(int G, bool sparse, bool select, const AttnArgs &a, int batch,
+                                 bool pdl, cudaStream_t stream);
+int attention_mma_ctas_per_sm(int G, bool sparse, bool select);
+
 // Preferred shared-memory carveout (percent, -1 = driver default) for later attention launches.
 void set_attention_carveout(int percent);
 

@@ -29,13 +29,19 @@ def orc():
     return oracle.get()
 
 
-@pytest.fixture(params=[0, 1], ids=["streamed", "staged"])
+PATHS = {"streamed": (0, 0, 0), "staged": (1, 1, 0), "mma": (0, 0, 1)}
+
+
+@pytest.fixture(params=list(PATHS))
 def staged(request):
-    td.td_set_tuning("full_staged", request.param)
-    td.td_set_tuning("sparse_staged", request.param)
+    full, sparse, mma = PATHS[request.param]
+    td.td_set_tuning("full_staged", full)
+    td.td_set_tuning("sparse_staged", sparse)
+    td.td_set_tuning("mma", mma)
     yield request.param
     td.td_set_tuning("full_staged", -1)
     td.td_set_tuning("sparse_staged", -1)
+    td.td_set_tuning("mma", -1)
 
 
 def _case(seed, B, Hq, Hkv, N, lens, layers, heavy_new=True):

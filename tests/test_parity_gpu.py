@@ -26,15 +26,23 @@ def _built():
     td.td_set_tuning("max_splits", 0)
 
 
-@pytest.fixture(scope="module", autouse=True, params=[0, 1], ids=["streamed", "staged"])
+PATHS = {"streamed": (0, 0, 0), "staged": (1, 1, 0), "mma": (0, 0, 1)}
+
+
+@pytest.fixture(scope="module", autouse=True, params=list(PATHS))
 def staged(request):
-    """Every case runs on both ways K/V rows reach the attention kernels:
-    register-streamed loads and bulk copies into shared-memory stages."""
-    td.td_set_tuning("full_staged", request.param)  # both paths for every G
-    td.td_set_tuning("sparse_staged", request.param)
+    """Every case runs on each kernel path: CUDA-core kernels with
+    register-streamed loads, the same with rows staged through shared memory,
+    and the tensor-core kernels (grouped-query layers with G = 4, 8; other
+    groups keep the CUDA-core kernels)."""
+    full, sparse, mma = PATHS[request.param]
+    td.td_set_tuning("full_staged", full)
+    td.td_set_tuning("sparse_staged", sparse)
+    td.td_set_tuning("mma", mma)
     yield request.param
     td.td_set_tuning("full_staged", -1)
     td.td_set_tuning("sparse_staged", -1)
+    td.td_set_tuning("mma", -1)
 
 
 @pytest.fixture(scope="module")
