@@ -12,10 +12,12 @@
 // Fragments come straight from global memory.  The dot product does not care
 // in which order the 128 dims are summed, so k-step j of the S product maps
 // MMA column pairs {2c, 2c+1} / {2c+8, 2c+9} of lane quad position c to dims
-// 32c + 4j + {0,1} / {2,3}: a lane then needs dims 32c .. 32c+31 of its token's
-// K row and of its head's q row (64 contiguous bytes each).  For O, MMA row r
-// / r+8 of m-tile i is dim 16r + 2i / 16r + 2i + 1, so a lane needs dims
-// 16r .. 16r+15 of two tokens' V rows; O is written back in natural order.
+// 16j + 4c + {0,1} / {2,3}: a lane reads 8 bytes of its token's K row (and of
+// its head's q row) per k-step, and a quad reads 32 contiguous bytes -- whole
+// sectors.  For O, MMA rows r / r+8 of m-tile i are the two dims of word i of
+// lane row r's V slice: dims 8r .. 8r+7 (tiles 0-3) and 64+8r .. 64+8r+7
+// (tiles 4-7), so 8 lanes read 128 contiguous bytes per load; O is written
+// back in natural order.
 //
 // P goes into the tensor cores as bf16, so it is split into three bf16 terms
 // (p = p1 + p2 + p3 to about 2^-24 relative) and O accumulates all three:
@@ -42,21 +44,24 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 16-byte read-only load that stays in L1: the four quarter-row pieces a
-// warp reads of one row arrive in neighbouring instructions.
+// 16-byte read-only load, no L1 allocation (8 lanes cover 128 contiguous bytes).
 __device__ __forceinline__ uint4 ldg16(const uint16_t *p)
 {
     uint4 r;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
     return r;
 }
 
-__device__ __forceinline__ uint32_t word(const uint4 (&v)[4], int w)
+// 8-byte read-only load (a quad covers whole 32-byte sectors per instruction).
+__device__ __forceinline__ uint2 ldg8(const uint16_t *p)
 {
-    const uint4 &x = v[w >> 2];
-    return (w & 3) == 0 ? x.x : (w & 3) == 1 ? x.y : (w & 3) == 2 ? x.z : x.w;
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(r.x), "=r"(r.y)
+                 : "l"(p));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t word2(const uint4 (&v)[2], int w)
@@ -129,52 +134,55 @@ attention_mma_kernel(const AttnArgs a)
     auto row_of = [&](int t) { return t < t1 ? (SPARSE ? sm_rows[t - t0] : t) : -1; };
 
     // This warp's 8 tokens of the round at `base`: K of token r (dims
-    // 32c..32c+31) and V of tokens 2c, 2c+1 (dims 16r..16r+15).
-    auto load = [&](int base, uint4 (&kq)[4], uint4 (&v0)[2], uint4 (&v1)[2]) {
+    // 16j + 4c .. +3 for k-step j) and V of tokens 2c, 2c+1 (dims 8r..8r+7 and
+    // 64+8r..64+8r+7).
+    auto load = [&](int base, uint2 (&kq)[8], uint4 (&v0)[2], uint4 (&v1)[2]) {
         const int tw = base + warp * 8;
         const int rk = row_of(tw + r);
         const int r0 = row_of(tw + 2 * c), r1 = row_of(tw + 2 * c + 1);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            kq[i] = rk >= 0 ? ldg16(kbase + (size_t)rk * kHeadDim + 32 * c + 8 * i)
-                            : make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < 8; ++j)
+            kq[j] = rk >= 0 ? ldg8(kbase + (size_t)rk * kHeadDim + 16 * j + 4 * c)
+                            : make_uint2(0u, 0u);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            v0[i] = r0 >= 0 ? ldg16(vbase + (size_t)r0 * kHeadDim + 16 * r + 8 * i)
+            v0[i] = r0 >= 0 ? ldg16(vbase + (size_t)r0 * kHeadDim + 64 * i + 8 * r)
                             : make_uint4(0u, 0u, 0u, 0u);
-            v1[i] = r1 >= 0 ? ldg16(vbase + (size_t)r1 * kHeadDim + 16 * r + 8 * i)
+            v1[i] = r1 >= 0 ? ldg16(vbase + (size_t)r1 * kHeadDim + 64 * i + 8 * r)
                             : make_uint4(0u, 0u, 0u, 0u);
         }
     };
-    uint4 kq0[4], va0[2], vb0[2];
+    uint2 kq0[8];
+    uint4 va0[2], vb0[2];
     load(t0, kq0, va0, vb0);  // the cache is never written by a kernel of the step
     pdl_wait();
 
-    // q of head r (heads >= G are zero columns): dims 32c..32c+31.
-    uint4 qf[4];
+    // q of head r (heads >= G are zero columns): dims 16j + 4c .. +3.
+    uint2 qf[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        qf[i] = r < G ? *reinterpret_cast<const uint4 *>(
-                            a.q + ((size_t)b * a.Hq + (size_t)g * G + r) * kHeadDim + 32 * c + 8 * i)
-                      : make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < 8; ++j)
+        qf[j] = r < G ? *reinterpret_cast<const uint2 *>(
+                            a.q + ((size_t)b * a.Hq + (size_t)g * G + r) * kHeadDim + 16 * j + 4 * c)
+                      : make_uint2(0u, 0u);
 
     const float c2 = a.scale * kLog2e;
     float m[2] = {-CUDART_INF_F, -CUDART_INF_F};  // heads 2c, 2c+1 (replicated over r)
     float l[2] = {0.0f, 0.0f};
-    float o[8][4];  // m-tile i: dims 16r+2i (0, 1: heads 2c, 2c+1) and 16r+2i+1 (2, 3)
+    // m-tile i holds dims vdim(i) (0, 1: heads 2c, 2c+1) and vdim(i) + 1 (2, 3),
+    // vdim(i) = (i < 4 ? 8r : 64 + 8r) + 2 (i % 4)
+    float o[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             o[i][j] = 0.0f;
 
-    auto round = [&](int base, const uint4 (&kq)[4], const uint4 (&v0)[2], const uint4 (&v1)[2]) {
+    auto round = [&](int base, const uint2 (&kq)[8], const uint4 (&v0)[2], const uint4 (&v1)[2]) {
         const int tw = base + warp * 8;
         float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            mma_bf16(s, word(kq, 2 * j), 0u, word(kq, 2 * j + 1), 0u, word(qf, 2 * j),
-                     word(qf, 2 * j + 1));
+            mma_bf16(s, kq[j].x, 0u, kq[j].y, 0u, qf[j].x, qf[j].y);
         const bool ok = row_of(tw + r) >= 0;
 
         if constexpr (SELECT) {
@@ -239,8 +247,8 @@ attention_mma_kernel(const AttnArgs a)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t w0 = word2(v0, i), w1 = word2(v1, i);
-            const uint32_t lo = prmt(w0, w1, 0x5410u);  // dim 16r+2i of tokens 2c, 2c+1
-            const uint32_t hi = prmt(w0, w1, 0x7632u);  // dim 16r+2i+1
+            const uint32_t lo = prmt(w0, w1, 0x5410u);  // dim vdim(i) of tokens 2c, 2c+1
+            const uint32_t hi = prmt(w0, w1, 0x7632u);  // dim vdim(i) + 1
 #pragma unroll
             for (int k = 0; k < 3; ++k)
                 mma_bf16(o[i], lo, hi, 0u, 0u, pb[k], 0u);
@@ -250,7 +258,8 @@ attention_mma_kernel(const AttnArgs a)
     if (t0 < t1)
         round(t0, kq0, va0, vb0);
     for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
-        uint4 kq[4], va[2], vb[2];
+        uint2 kq[8];
+        uint4 va[2], vb[2];
         load(base, kq, va, vb);
         round(base, kq, va, vb);
     }
@@ -268,8 +277,9 @@ attention_mma_kernel(const AttnArgs a)
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                sm_o[warp][h][16 * r + 2 * i] = o[i][e];
-                sm_o[warp][h][16 * r + 2 * i + 1] = o[i][e + 2];
+                const int d = (i < 4 ? 8 * r : 64 + 8 * r) + 2 * (i & 3);
+                sm_o[warp][h][d] = o[i][e];
+                sm_o[warp][h][d + 1] = o[i][e + 2];
             }
         }
     }
