@@ -280,12 +280,19 @@ def coverage_layer(td, torch, wl, shape, q, K, V, seq, ws, device, flush_l2, str
 
 
 # ----------------------------------------------------------------- our arm
+def apply_tuning(td, pairs):
+    for kv in pairs:
+        key, _, value = kv.partition("=")
+        td.td_set_tuning(key, int(value))
+
+
 def run_ours(args, world, rank, local):
     import torch
     import sparse_attention_td_gb300 as td
     if not os.path.exists(td.lib_path()):
         import __graft_entry__
         __graft_entry__.build()
+    apply_tuning(td, args.tuning)
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     dist_init(world, "nccl")
@@ -659,6 +666,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", choices=["full", "select", "sparse"], default=None,
                     help="time one layer's launch alone (small case for ncu)")
+    ap.add_argument("--tuning", action="append", default=[], metavar="KEY=VALUE",
+                    help="td_set_tuning before running (repeatable), e.g. mma=0")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -337,9 +337,10 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          the tensor cores (mma.sync over the group's heads); 0 on the CUDA
  *          cores (where "full_staged" / "sparse_staged" apply); negative
  *          restores the default
- *   "topk_threads": 1024 or 512 threads per top-k row; other values restore
- *                   the default (1024 when batch * kv_heads fits one wave of
- *                   one CTA per SM, else 512 with two CTAs per SM)
+ *   "topk_threads": 1024 (default) or 512 threads per top-k row (512: two
+ *                   CTAs per SM); other values restore the default
+ *   "pdl", "topk_pdl": 0 turns off programmatic dependent launch between a
+ *                   call's kernels / before the top-k kernel (default 1)
  * Otherwise value <= 0 restores the default.  Unknown key -> TD_ERR_INVALID_ARG.
  */
 td_status td_set_tuning(const char *key, int32_t value);

@@ -29,12 +29,14 @@ struct Tuning {
     int sparse_waves = 1;
     int max_splits = td::kMaxSplits;
     int cluster = 0;             // 1: merge up to kPortableClusterSplits splits through a cluster
-    int topk_threads = 0;        // 0 = by row count, else 512 or 1024
+    int topk_threads = 0;        // 0 = 1024 threads per row, or 512
     int full_staged = -1;        // 1: full / full+select kernels stage K/V through shared memory
                                  // (bulk copies); 0: register-streamed; -1: staged when G >= 4
     int sparse_staged = 0;       // 1: sparse kernels stage the gathered rows through shared memory
                                  // (per-thread cp.async ring); 0: register-streamed
     int mma = -1;                // 1 / -1 (default): tensor-core kernels for G = 4, 8; 0: CUDA cores
+    int pdl = 1;                 // 0: no programmatic dependent launch between a call's kernels
+    int topk_pdl = 1;            // 0: the top-k kernel waits for its attention kernel in stream order
 };
 Tuning g_tuning;
 const Tuning kDefaultTuning;
@@ -328,12 +330,13 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
             ca.Nmax = c.shape.max_seq_len;
             ca.kcap = top_k;
             ca.tau = cov.tau;
-            if (td::launch_coverage(ca, c.shape.batch, true, st) != cudaSuccess)
+            if (td::launch_coverage(ca, c.shape.batch, g_tuning.pdl != 0, st) != cudaSuccess)
                 return TD_ERR_CUDA;
             t.row_k = ca.row_k;
             t.counts = cov.counts;
         }
-        if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, true, st) != cudaSuccess)
+        if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads,
+                            g_tuning.pdl != 0 && g_tuning.topk_pdl != 0, st) != cudaSuccess)
             return TD_ERR_CUDA;
     }
     return TD_OK;
@@ -427,7 +430,7 @@ td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
             return TD_ERR_CUDA;
     }
     for (int l = 0; l < num_layers; ++l) {
-        const bool pdl = l > 0;  // the first kernel waits for whatever precedes it
+        const bool pdl = l > 0 && g_tuning.pdl;  // the first kernel waits for what precedes it
         if (layer_events && layer_events[l] &&
             cudaEventRecord((cudaEvent_t)layer_events[l], st) != cudaSuccess)
             return TD_ERR_CUDA;
@@ -801,6 +804,10 @@ td_status td_set_tuning(const char *key, int32_t value)
         g_tuning.sparse_staged = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.sparse_staged);
     else if (!strcmp(key, "mma"))
         g_tuning.mma = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.mma);
+    else if (!strcmp(key, "pdl"))
+        g_tuning.pdl = value != 0 ? 1 : 0;
+    else if (!strcmp(key, "topk_pdl"))
+        g_tuning.topk_pdl = value != 0 ? 1 : 0;
     else if (!strcmp(key, "topk_threads"))
         g_tuning.topk_threads = (value == 512 || value == 1024) ? value : 0;
     else if (!strcmp(key, "attn_carveout"))

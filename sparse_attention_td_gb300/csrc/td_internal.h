@@ -87,8 +87,7 @@ struct CoverageArgs {
 // kernel of the same call.
 cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, bool staged,
                              const AttnArgs &a, int batch, bool pdl, cudaStream_t stream);
-// threads: 1024 or 512 threads per row's CTA; 0 picks 1024 when the rows fit
-// one wave on the device's SMs, else 512 (two CTAs per SM).
+// threads: 1024 or 512 threads per row's CTA (0: 1024).
 cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, bool pdl,
                         cudaStream_t stream);
 cudaError_t launch_coverage(const CoverageArgs &a, int batch, bool pdl, cudaStream_t stream);

@@ -126,6 +126,10 @@ def test_tuning_keys(L):
     td.td_set_tuning("full_waves", 0)     # default again
     td.td_set_tuning("topk_threads", 512)
     td.td_set_tuning("topk_threads", 0)
+    td.td_set_tuning("pdl", 0)
+    td.td_set_tuning("pdl", 1)
+    td.td_set_tuning("mma", 0)
+    td.td_set_tuning("mma", -1)
     with pytest.raises(td.TdError):
         td.td_set_tuning("no_such_knob", 1)
 
