@@ -203,7 +203,7 @@ def load_measured_peaks():
 
 def attn_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("td_attn.cu", "td_internal.h"):
+    for name in ("td_attn.cu", "td_attn_mma.cu", "td_attn_common.cuh", "td_internal.h"):
         with open(os.path.join(ROOT, "sparse_attention_td_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
