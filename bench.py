@@ -193,6 +193,20 @@ def time_oracle(wl: W.Workload, sample, modes):
 
 
 # ----------------------------------------------------------------- helpers
+def host_cpu_name() -> str:
+    """CPU model from /proc/cpuinfo ("model name", else the Arm part number)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "CPU part"):
+        for ln in lines:
+            if ln.startswith(key):
+                return f"{key}: {ln.split(':', 1)[1].strip()}"
+    return "unknown"
+
+
 def load_measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -557,6 +571,20 @@ def run_ours(args, world, rank, local):
             "sample": f"{len(pick)} of {groups} (batch row, KV head) groups through all "
                       f"{wl.layers} layers, x{reps} runs, scaled to the whole step",
         }
+        # the same oracle on one thread, on a smaller sample (same scaling)
+        import oracle
+        orc = oracle.get()
+        one = pick[:max(1, len(pick) // 8)]
+        sample1 = host_sample(layers, wl, lens, one)
+        orc.set_threads(1)
+        try:
+            dt1, _ = time_oracle(wl, sample1, modes)
+        finally:
+            orc.set_threads(threads)
+        result["cpu_baseline"].update({
+            "value_1_thread": round(dt1 * (groups / len(one)) * 1e6, 1),
+            "sample_1_thread": f"{len(one)} of {groups} groups, one run, scaled",
+            "host_cpus": os.cpu_count(), "host_cpu": host_cpu_name()})
     return result
 
 

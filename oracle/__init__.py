@@ -117,6 +117,8 @@ class Oracle:
         L.oracle_coverage_count.argtypes = [f64p, ctypes.c_int, ctypes.c_double, ctypes.c_int]
         L.oracle_mutant_id.restype = ctypes.c_int
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_set_threads.restype = None
+        L.oracle_set_threads.argtypes = [ctypes.c_int]
 
     # -- single pieces -------------------------------------------------------
     def bf16_to_double(self, bits: int) -> float:
@@ -247,6 +249,10 @@ class Oracle:
 
     def mutant_id(self) -> int:
         return self._lib.oracle_mutant_id()
+
+    def set_threads(self, n: int) -> None:
+        """Threads the OpenMP regions use from now on (1 = serial)."""
+        self._lib.oracle_set_threads(int(n))
 
     def num_threads(self) -> int:
         return self._lib.oracle_num_threads()

@@ -485,6 +485,9 @@ int oracle_mutant_id(void) { return ORACLE_MUTANT; }
 #ifdef _OPENMP
 #include <omp.h>
 int oracle_num_threads(void) { return omp_get_max_threads(); }
+/* Threads for later parallel regions (n >= 1). */
+void oracle_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
 #else
 int oracle_num_threads(void) { return 1; }
+void oracle_set_threads(int n) { (void)n; }
 #endif
