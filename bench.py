@@ -636,6 +636,7 @@ def run_profile_layer(args, local):
     if not os.path.exists(td.lib_path()):
         import __graft_entry__
         __graft_entry__.build()
+    apply_tuning(td, args.tuning)
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     wl = W.WORKLOADS[args.config]

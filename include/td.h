@@ -337,6 +337,10 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          the tensor cores (mma.sync over the group's heads); 0 on the CUDA
  *          cores (where "full_staged" / "sparse_staged" apply); negative
  *          restores the default
+ *   "full_prefetch": 0..4 rounds ahead whose K/V lines each warp of a
+ *          register-streamed full or full+select kernel prefetches into L2;
+ *          negative restores the default (1 on the tensor cores, 0 on the
+ *          CUDA cores)
  *   "topk_threads": 1024 (default) or 512 threads per top-k row (512: two
  *                   CTAs per SM); other values restore the default
  *   "pdl", "topk_pdl": 0 turns off programmatic dependent launch between a

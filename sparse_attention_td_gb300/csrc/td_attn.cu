@@ -285,6 +285,12 @@ attention_kernel(const AttnArgs a)
     } else {
         load_round(t0, kr0, vr0, ok0);
     }
+    // register-streamed full layers: rounds 1 .. prefetch go to L2 now, later
+    // rounds `prefetch` ahead of use
+    auto row_at = [&](int t) { return t < t1 ? t : -1; };
+    const int pf = (STAGED || SPARSE) ? 0 : a.prefetch;
+    for (int d = 1; d <= pf; ++d)
+        prefetch_round_l2(krows, vrows, t0 + d * kTokPerRound + warp * 8, lane, row_at);
     pdl_wait();
 
     // This lane's 8 dims of the group's G queries, as 4 dim pairs.
@@ -484,6 +490,8 @@ attention_kernel(const AttnArgs a)
         for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
             uint4 kr[U], vr[U];
             bool ok[U];
+            if (pf > 0)
+                prefetch_round_l2(krows, vrows, base + pf * kTokPerRound + warp * 8, lane, row_at);
             load_round(base, kr, vr, ok);
             round(base, kr, vr, ok);
         }

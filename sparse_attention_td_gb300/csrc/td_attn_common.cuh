@@ -45,6 +45,20 @@ __device__ __forceinline__ uint4 load_row16(const uint16_t *p)
 // earlier than by the kernel right before); after it, everything the
 // previous kernel wrote (q in a full model, index set, scores, workspace) is
 // complete and visible.
+// L2 prefetch of the K and V rows a warp takes in one round: its 8 tokens
+// starting at `tw`, one 128-byte line per lane (lanes 0-15 K, 16-31 V, two
+// lines per row).  `row_of(t)` gives a token's cache row, or -1 to skip it.
+template <typename RowOf>
+__device__ __forceinline__ void prefetch_round_l2(const uint16_t *kbase, const uint16_t *vbase,
+                                                  int tw, int lane, RowOf row_of)
+{
+    const int row = row_of(tw + ((lane >> 1) & 7));
+    if (row >= 0) {
+        const uint16_t *p = (lane < 16 ? kbase : vbase) + (size_t)row * kHeadDim + (lane & 1) * 64;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+}
+
 __device__ __forceinline__ void pdl_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -155,6 +155,11 @@ attention_mma_kernel(const AttnArgs a)
     uint2 kq0[8];
     uint4 va0[2], vb0[2];
     load(t0, kq0, va0, vb0);  // the cache is never written by a kernel of the step
+    // full layers: rounds 1 .. prefetch go to L2 now, later rounds `prefetch`
+    // ahead of use (measured on GB300: no gain for gathered rows)
+    const int pf = SPARSE ? 0 : a.prefetch;
+    for (int d = 1; d <= pf; ++d)
+        prefetch_round_l2(kbase, vbase, t0 + d * kTokPerRound + warp * 8, lane, row_of);
     pdl_wait();
 
     // q of head r (heads >= G are zero columns): dims 16j + 4c .. +3.
@@ -260,6 +265,8 @@ attention_mma_kernel(const AttnArgs a)
     for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
         uint2 kq[8];
         uint4 va[2], vb[2];
+        if (pf > 0)
+            prefetch_round_l2(kbase, vbase, base + pf * kTokPerRound + warp * 8, lane, row_of);
         load(base, kq, va, vb);
         round(base, kq, va, vb);
     }

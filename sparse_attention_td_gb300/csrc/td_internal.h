@@ -50,6 +50,7 @@ struct AttnArgs {
     int idx_dep;             // sparse: the index set may be written by the previous kernel
     int chunk;               // tokens (full) or index entries (sparse) per split
     int nsplit;              // gridDim.x
+    int prefetch;            // full layers: rounds ahead whose rows each warp prefetches into L2 (0: none)
     float scale;             // softmax scale (natural-log units)
 };
 

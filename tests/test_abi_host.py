@@ -130,6 +130,8 @@ def test_tuning_keys(L):
     td.td_set_tuning("pdl", 1)
     td.td_set_tuning("mma", 0)
     td.td_set_tuning("mma", -1)
+    td.td_set_tuning("full_prefetch", 2)
+    td.td_set_tuning("full_prefetch", -1)
     with pytest.raises(td.TdError):
         td.td_set_tuning("no_such_knob", 1)
 

@@ -29,19 +29,22 @@ def orc():
     return oracle.get()
 
 
-PATHS = {"streamed": (0, 0, 0), "staged": (1, 1, 0), "mma": (0, 0, 1)}
+PATHS = {"streamed": (0, 0, 0, -1), "staged": (1, 1, 0, -1), "mma": (0, 0, 1, -1),
+         "prefetch2": (0, 0, 1, 2)}
 
 
 @pytest.fixture(params=list(PATHS))
 def staged(request):
-    full, sparse, mma = PATHS[request.param]
+    full, sparse, mma, prefetch = PATHS[request.param]
     td.td_set_tuning("full_staged", full)
     td.td_set_tuning("sparse_staged", sparse)
     td.td_set_tuning("mma", mma)
+    td.td_set_tuning("full_prefetch", prefetch)
     yield request.param
     td.td_set_tuning("full_staged", -1)
     td.td_set_tuning("sparse_staged", -1)
     td.td_set_tuning("mma", -1)
+    td.td_set_tuning("full_prefetch", -1)
 
 
 def _case(seed, B, Hq, Hkv, N, lens, layers, heavy_new=True):

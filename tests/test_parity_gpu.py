@@ -26,7 +26,8 @@ def _built():
     td.td_set_tuning("max_splits", 0)
 
 
-PATHS = {"streamed": (0, 0, 0), "staged": (1, 1, 0), "mma": (0, 0, 1)}
+PATHS = {"streamed": (0, 0, 0, -1), "staged": (1, 1, 0, -1), "mma": (0, 0, 1, -1),
+         "prefetch2": (0, 0, 1, 2)}
 
 
 @pytest.fixture(scope="module", autouse=True, params=list(PATHS))
@@ -34,15 +35,19 @@ def staged(request):
     """Every case runs on each kernel path: CUDA-core kernels with
     register-streamed loads, the same with rows staged through shared memory,
     and the tensor-core kernels (grouped-query layers with G = 4, 8; other
-    groups keep the CUDA-core kernels)."""
-    full, sparse, mma = PATHS[request.param]
+    groups keep the CUDA-core kernels); and the last with full layers
+    prefetching two rounds ahead into L2 (the default is one round on the
+    tensor cores, none on the CUDA cores)."""
+    full, sparse, mma, prefetch = PATHS[request.param]
     td.td_set_tuning("full_staged", full)
     td.td_set_tuning("sparse_staged", sparse)
     td.td_set_tuning("mma", mma)
+    td.td_set_tuning("full_prefetch", prefetch)
     yield request.param
     td.td_set_tuning("full_staged", -1)
     td.td_set_tuning("sparse_staged", -1)
     td.td_set_tuning("mma", -1)
+    td.td_set_tuning("full_prefetch", -1)
 
 
 @pytest.fixture(scope="module")
