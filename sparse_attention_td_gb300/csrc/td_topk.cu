@@ -393,7 +393,10 @@ topk_kernel(const TopkArgs a)
         const int vec_n = (((uintptr_t)s & 15u) == 0) ? n / 4 : 0;  // whole float4 groups
         // Aligned rows: a thread takes 4 consecutive scores per load, so a warp
         // covers 128 positions = 4 bitmap words (a word's 8 nibbles are OR-ed
-        // together with 3 shuffles) and appends its candidates after one warp scan.
+        // together with 3 shuffles).  A key is in the threshold bin (above it)
+        // when its first digit equals (exceeds) d1.  The bin holds a few
+        // percent of the row at most, so each hit takes its candidate slot
+        // with its own shared-memory atomic: no per-group warp scan.
         for (int base = 0; base < vec_n; base += kT * kBatchV) {
             float4 v[kBatchV];
 #pragma unroll
@@ -413,8 +416,9 @@ topk_kernel(const TopkArgs a)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     key[e] = order_key(f[e]);
-                    hitm |= (live && (key[e] & mask1) == prefix1) ? (1u << e) : 0u;
-                    abovem |= (live && key[e] > top_of_bin) ? (1u << e) : 0u;
+                    const uint32_t dg = key[e] >> (32 - kBits1);
+                    hitm |= (live && dg == d1) ? (1u << e) : 0u;
+                    abovem |= (live && dg > d1) ? (1u << e) : 0u;
                 }
                 if (use_bitmap) {
                     unsigned word = abovem << (4 * (lane & 7));
@@ -424,26 +428,13 @@ topk_kernel(const TopkArgs a)
                     if ((lane & 7) == 0 && live)
                         sm.bitmap[pos0 >> 5] = word;
                 }
-                const unsigned cnt = __popc(hitm);
-                unsigned incl = cnt;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const unsigned t = __shfl_up_sync(kFull, incl, off);
-                    if (lane >= off)
-                        incl += t;
-                }
-                const unsigned total = __shfl_sync(kFull, incl, 31);
-                if (total) {  // warp-uniform
-                    unsigned slot0 = 0;
-                    if (lane == 0)
-                        slot0 = atomicAdd(&sm.cand_count, total);
-                    unsigned slot = __shfl_sync(kFull, slot0, 0) + incl - cnt;
+                if (hitm) {  // at most bin_count <= kCand hits in all: slots stay in range
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         if (hitm & (1u << e)) {
+                            const unsigned slot = atomicAdd(&sm.cand_count, 1u);
                             cand_key[slot] = key[e];
                             cand_pos[slot] = pos0 + e;
-                            ++slot;
                         }
                 }
             }
