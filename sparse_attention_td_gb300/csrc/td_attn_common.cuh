@@ -1,8 +1,9 @@
 // td_attn_common.cuh -- device helpers shared by the attention kernels
 // (register/shared-memory paths in td_attn.cu, tensor-core path in
-// td_attn_mma.cu): launch-dependency waits, score keys, and the last stage of
-// a split-K launch (a CTA's normalised partial result, the split merge by
-// the last-arriving CTA of a (batch row, KV head)).
+// td_attn_mma.cu): launch-dependency waits, the score key, L2 prefetch, and
+// the last stage of a split-K launch (a CTA's normalised partial result, the
+// split merge by the last-arriving CTA of a (batch row, KV head)).  The top-k
+// kernels (td_topk.cu) use the same score key and waits.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -69,8 +70,8 @@ __device__ __forceinline__ void pdl_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Order-preserving 32-bit key of a score (as in the top-k kernel): larger
-// float -> larger unsigned, -0.0 equal to +0.0.
+// Order-preserving 32-bit key of a score, shared with the top-k kernel:
+// larger float -> larger unsigned; -0.0 is mapped to +0.0 first so the two tie.
 __device__ __forceinline__ uint32_t order_key(float f)
 {
     uint32_t u = __float_as_uint(f);

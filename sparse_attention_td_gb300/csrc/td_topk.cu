@@ -29,12 +29,14 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "td_attn_common.cuh"  // order_key (the attention kernels' first-digit
+                               // histogram bins scores with the same key),
+                               // launch-dependency waits
 #include "td_internal.h"
 
 namespace td {
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBatch = 16;              // loads in flight per thread
 constexpr int kBatchV = 4;              // float4 loads in flight per thread (16 scores)
 constexpr unsigned kWarpSelectMax = 2048; // threshold bins up to this size finish in one warp
@@ -43,28 +45,9 @@ constexpr int kBins1 = kSelectBins;     // 2048
 constexpr int kBitmapWords = kTopkBitmapBits / 32;
 constexpr int kSubHists = 4;            // pass-1 sub-histograms (less atomic contention)
 
-// Programmatic dependent launch (see td_attn.cu): the scores come from the
-// kernel just before this one, so wait for it; the next layer's kernel may
+// Programmatic dependent launch: the scores come from the kernel just before
+// this one, so the kernel waits for it (pdl_wait); the next layer's kernel may
 // launch right away (it waits for this one before reading the index set).
-__device__ __forceinline__ void pdl_wait()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Order-preserving key: larger float -> larger unsigned.  -0.0 is mapped to
-// +0.0 first so the two tie.
-__device__ __forceinline__ uint32_t order_key(float f)
-{
-    uint32_t u = __float_as_uint(f);
-    if (u == 0x80000000u)
-        u = 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // The kernel is instantiated for two block sizes: 1024 threads (one CTA per
 // SM, for launches with fewer rows than SMs) and 512 threads (two CTAs per SM
