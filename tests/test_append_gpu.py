@@ -29,22 +29,22 @@ def orc():
     return oracle.get()
 
 
-PATHS = {"streamed": (0, 0, 0, -1), "staged": (1, 1, 0, -1), "mma": (0, 0, 1, -1),
-         "prefetch2": (0, 0, 1, 2)}
+PATHS = {
+    "streamed": {"full_staged": 0, "sparse_staged": 0, "mma": 0},
+    "staged": {"full_staged": 1, "sparse_staged": 1, "mma": 0},
+    "mma": {"mma": 1},
+    "prefetch2": {"mma": 1, "full_prefetch": 2},
+}
+TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch")
 
 
 @pytest.fixture(params=list(PATHS))
 def staged(request):
-    full, sparse, mma, prefetch = PATHS[request.param]
-    td.td_set_tuning("full_staged", full)
-    td.td_set_tuning("sparse_staged", sparse)
-    td.td_set_tuning("mma", mma)
-    td.td_set_tuning("full_prefetch", prefetch)
+    for key, value in PATHS[request.param].items():
+        td.td_set_tuning(key, value)
     yield request.param
-    td.td_set_tuning("full_staged", -1)
-    td.td_set_tuning("sparse_staged", -1)
-    td.td_set_tuning("mma", -1)
-    td.td_set_tuning("full_prefetch", -1)
+    for key in TUNING_KEYS:
+        td.td_set_tuning(key, -1)
 
 
 def _case(seed, B, Hq, Hkv, N, lens, layers, heavy_new=True):

@@ -26,8 +26,13 @@ def _built():
     td.td_set_tuning("max_splits", 0)
 
 
-PATHS = {"streamed": (0, 0, 0, -1), "staged": (1, 1, 0, -1), "mma": (0, 0, 1, -1),
-         "prefetch2": (0, 0, 1, 2)}
+PATHS = {
+    "streamed": {"full_staged": 0, "sparse_staged": 0, "mma": 0},
+    "staged": {"full_staged": 1, "sparse_staged": 1, "mma": 0},
+    "mma": {"mma": 1},
+    "prefetch2": {"mma": 1, "full_prefetch": 2},
+}
+TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch")
 
 
 @pytest.fixture(scope="module", autouse=True, params=list(PATHS))
@@ -35,19 +40,14 @@ def staged(request):
     """Every case runs on each kernel path: CUDA-core kernels with
     register-streamed loads, the same with rows staged through shared memory,
     and the tensor-core kernels (grouped-query layers with G = 4, 8; other
-    groups keep the CUDA-core kernels); and the last with full layers
+    groups keep the CUDA-core kernels); and the same with full layers
     prefetching two rounds ahead into L2 (the default is one round on the
     tensor cores, none on the CUDA cores)."""
-    full, sparse, mma, prefetch = PATHS[request.param]
-    td.td_set_tuning("full_staged", full)
-    td.td_set_tuning("sparse_staged", sparse)
-    td.td_set_tuning("mma", mma)
-    td.td_set_tuning("full_prefetch", prefetch)
+    for key, value in PATHS[request.param].items():
+        td.td_set_tuning(key, value)
     yield request.param
-    td.td_set_tuning("full_staged", -1)
-    td.td_set_tuning("sparse_staged", -1)
-    td.td_set_tuning("mma", -1)
-    td.td_set_tuning("full_prefetch", -1)
+    for key in TUNING_KEYS:
+        td.td_set_tuning(key, -1)
 
 
 @pytest.fixture(scope="module")
