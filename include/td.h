@@ -341,6 +341,9 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          register-streamed full or full+select kernel prefetches into L2;
  *          negative restores the default (1 on the tensor cores, 0 on the
  *          CUDA cores)
+ *   "topk_warp_max": top-k threshold bins of up to this many candidates are
+ *          finished by one warp, larger ones by block-wide radix passes
+ *          (default 256)
  *   "topk_threads": 1024 (default) or 512 threads per top-k row (512: two
  *                   CTAs per SM); other values restore the default
  *   "pdl", "topk_pdl": 0 turns off programmatic dependent launch between a

@@ -37,6 +37,7 @@ struct Tuning {
     int mma = -1;                // 1 / -1 (default): tensor-core kernels for G = 4, 8; 0: CUDA cores
     int full_prefetch = -1;      // full / full+select layers: rounds ahead each warp prefetches into
                                  // L2 (register-streamed kernels); -1: 1 on the tensor cores, else 0
+    int topk_warp_max = 0;       // top-k threshold bins up to this size finish in one warp (0: 256)
     int pdl = 1;                 // 0: no programmatic dependent launch between a call's kernels
     int topk_pdl = 1;            // 0: the top-k kernel waits for its attention kernel in stream order
 };
@@ -329,6 +330,7 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
         t.Hkv = c.shape.num_kv_heads;
         t.Nmax = c.shape.max_seq_len;
         t.top_k = top_k;
+        t.warp_select_max = g_tuning.topk_warp_max;
         if (cov.tau >= 0.0f) {
             td::CoverageArgs ca{};
             ca.scores = a.scores;
@@ -588,6 +590,7 @@ td_status td_topk_select(const td_shape *shape, const float *scores, const int32
     t.Hkv = c.shape.num_kv_heads;
     t.Nmax = c.shape.max_seq_len;
     t.top_k = top_k;
+    t.warp_select_max = g_tuning.topk_warp_max;
     if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, false, (cudaStream_t)stream) !=
         cudaSuccess)
         return TD_ERR_CUDA;
@@ -817,6 +820,8 @@ td_status td_set_tuning(const char *key, int32_t value)
         g_tuning.mma = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.mma);
     else if (!strcmp(key, "full_prefetch"))
         g_tuning.full_prefetch = (value >= 0 && value <= 4) ? value : kDefaultTuning.full_prefetch;
+    else if (!strcmp(key, "topk_warp_max"))
+        g_tuning.topk_warp_max = value > 0 ? value : kDefaultTuning.topk_warp_max;
     else if (!strcmp(key, "pdl"))
         g_tuning.pdl = value != 0 ? 1 : 0;
     else if (!strcmp(key, "topk_pdl"))

@@ -63,6 +63,7 @@ struct TopkArgs {
     const int32_t *row_k;    // [B*Hkv] per-row budget (<= top_k), or null: top_k for every row
     int32_t *counts;         // [B*Hkv] positions selected per row (min(k, N_b)), or null
     int Hkv, Nmax, top_k;
+    int warp_select_max;     // threshold bins up to this many pairs finish in one warp (0: the default, 256)
 };
 
 // Coverage budget per (batch row, KV head): row_k[bg] = min(kcap, smallest k

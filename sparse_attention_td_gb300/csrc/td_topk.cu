@@ -39,7 +39,11 @@ namespace {
 
 constexpr int kBatch = 16;              // loads in flight per thread
 constexpr int kBatchV = 4;              // float4 loads in flight per thread (16 scores)
-constexpr unsigned kWarpSelectMax = 2048; // threshold bins up to this size finish in one warp
+// Threshold bins up to this size finish in one warp (no block barriers);
+// larger ones take block-wide radix passes.  Measured on GB300: 256 beats
+// 2048 by 1-4 us per selection layer on 10K-32K rows, whose bins hold
+// several hundred to ~2000 pairs (one warp makes a serial pass per 32).
+constexpr unsigned kWarpSelectMax = 256;
 constexpr int kBits1 = kSelectBits;     // first digit: key bits 31..21
 constexpr int kBins1 = kSelectBins;     // 2048
 constexpr int kBitmapWords = kTopkBitmapBits / 32;
@@ -454,7 +458,8 @@ topk_kernel(const TopkArgs a)
         }
         __syncthreads();
         const unsigned cnt = sm.cand_count;
-        if (use_bitmap && cnt <= kWarpSelectMax) {
+        const unsigned warp_max = a.warp_select_max > 0 ? (unsigned)a.warp_select_max : kWarpSelectMax;
+        if (use_bitmap && cnt <= warp_max) {
             // small threshold bin: one warp finishes the select and marks the
             // selected candidates, without block-wide barriers
             if (warp == 0) {

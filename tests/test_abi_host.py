@@ -132,6 +132,8 @@ def test_tuning_keys(L):
     td.td_set_tuning("mma", -1)
     td.td_set_tuning("full_prefetch", 2)
     td.td_set_tuning("full_prefetch", -1)
+    td.td_set_tuning("topk_warp_max", 2048)
+    td.td_set_tuning("topk_warp_max", 0)
     with pytest.raises(td.TdError):
         td.td_set_tuning("no_such_knob", 1)
 

@@ -55,12 +55,17 @@ def orc():
     return oracle.get()
 
 
-@pytest.fixture(params=[1024, 512])
+@pytest.fixture(params=[(1024, 0), (512, 0), (1024, 2048)], ids=["t1024", "t512", "t1024-warp2048"])
 def topk_threads(request):
-    """Both block sizes of the top-k kernel (the default picks by row count)."""
-    td.td_set_tuning("topk_threads", request.param)
-    yield request.param
+    """Both block sizes of the top-k kernel, and the threshold-bin select taken
+    by one warp up to 2048 candidates instead of the default 256 (so the
+    adversarial rows run through both select paths)."""
+    threads, warp_max = request.param
+    td.td_set_tuning("topk_threads", threads)
+    td.td_set_tuning("topk_warp_max", warp_max)
+    yield threads
     td.td_set_tuning("topk_threads", 0)
+    td.td_set_tuning("topk_warp_max", 0)
 
 
 def _dev(*ts):
