@@ -197,6 +197,23 @@ def test_topk_large_rows(orc, topk_threads):
         assert np.array_equal(got[b, 0], want), f"row {b}"
 
 
+def test_topk_rows_longer_than_the_bitmap(orc):
+    """Rows up to 2^18 positions are written through a shared-memory bitmap;
+    longer ones take the ordered-compaction path.  Lengths at, just past and
+    well past the boundary, with heavy ties at the k-th score."""
+    rs = np.random.RandomState(8)
+    N = 300000
+    rows = [rs.randn(N).astype(np.float32),
+            np.round(rs.randn(N) * 4).astype(np.float32),
+            np.round(rs.randn(N) * 4).astype(np.float32)]
+    lens = [N, 1 << 18, (1 << 18) + 1]
+    for k in (1, 4096, 100000):
+        arr, got = _topk_case(rows, lens, k)
+        for b in range(len(rows)):
+            want = orc.topk(arr[b, 0, :lens[b]].astype(np.float64), k)
+            assert np.array_equal(got[b, 0], want), f"row {b} k={k}"
+
+
 def test_topk_threshold_bin_larger_than_shared_memory(orc, topk_threads):
     """More than 16384 (512-thread CTAs: 8192) scores share the threshold's
     top bits: the kernel's streaming fallback path (heavy ties at and around
