@@ -6,8 +6,10 @@
 One "step" is one decode step of the whole L-layer attention-only stack
 (full, full+select and sparse layers per the review's Figure 2 schedule) over
 one batch of synthetic, seeded inputs resident in HBM.  Default workload: the
-LLaMA-2-7B attention shape at 10K context (batch 1, 32 layers, 32 heads,
-d=128, N=10240, k=512, selection at L2 and L7).
+largest single-GPU configuration, the long-context LLaMA-2-7B attention shape
+(batch 1, 32 layers, 32 heads, d=128, N=102400, k=4096, selection at L2 and
+L7; 53.7 GB of K/V resident).  The 10K, 32K and serving shapes run through
+--config.
 
 Timing: W untimed warm-up steps, then exactly K timed steps, each preceded by
 an L2 flush (a 1 GiB device write, outside the timed events), timed with CUDA
@@ -41,7 +43,7 @@ if ROOT not in sys.path:
 import workloads as W  # noqa: E402
 
 METRIC = ("decode-step attention latency (us) and achieved KV HBM GB/s vs peak, PPSA vs full")
-DEFAULT_CONFIG = "llama2-7b-10k"
+DEFAULT_CONFIG = "llama2-7b-100k"
 FLUSH_BYTES = 1 << 30
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the roofline uses the measured copy peak)
@@ -99,32 +101,50 @@ def step_bytes(wl: W.Workload, lens: np.ndarray, modes) -> dict:
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clock/throttle samples while the timed region runs."""
+    """nvidia-smi clock/throttle samples while the timed region runs.
+
+    Samples every `interval_ms`; on entry it waits (at most `first_wait_s`)
+    for the first sample, so that the sampler is already running when the
+    timed region starts.  The summary counts only samples taken between
+    mark_start() and mark_stop() (the whole region when neither is called)."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 20, first_wait_s: float = 5.0):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
+        self.first_wait_s = first_wait_s
         self.proc = None
-        self.lines = []
+        self.lines = []      # (host time, csv line)
+        self.t_start = None
+        self.t_stop = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            t0 = time.perf_counter()
+            while not self.lines and time.perf_counter() - t0 < self.first_wait_s:
+                time.sleep(0.01)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.perf_counter()
+
+    def mark_stop(self):
+        self.t_stop = time.perf_counter()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -138,7 +158,11 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lo = self.t_start if self.t_start is not None else -math.inf
+        hi = self.t_stop if self.t_stop is not None else math.inf
+        for t, ln in self.lines:
+            if not lo <= t <= hi:
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -153,11 +177,20 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "interval_ms": self.interval_ms}
 
 
 # ----------------------------------------------------------------- oracle timing
+HOST_SAMPLE_BYTES = 8 << 30  # host copies of the oracle's sample stay below this
+
+
 def pick_groups(wl: W.Workload, n_groups: int):
+    """Seeded sample of (batch row, KV head) groups for the oracle: at most
+    n_groups, and no more than HOST_SAMPLE_BYTES of host K/V copies (a group
+    carries every layer's K and V rows)."""
+    per_group = wl.layers * wl.max_seq_len * wl.head_dim * 2 * 2
+    n_groups = max(1, min(n_groups, HOST_SAMPLE_BYTES // per_group))
     rs = np.random.RandomState(wl.seed + 5)
     all_groups = [(b, g) for b in range(wl.batch) for g in range(wl.kv_heads)]
     n = min(n_groups, len(all_groups))
@@ -336,6 +369,13 @@ def run_ours(args, world, rank, local):
     plan = td.Plan(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
     plan_full = td.Plan(shape, full_modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
     plan_sel = td.Plan(shape, sel_modes, q, K, V, seq, wl.top_k, idx, outs, None, ws)
+    # the same step without its sparse layers: the PPSA step minus this one is
+    # what the sparse layers cost inside the graph step (their overlap with
+    # neighbouring layers included, which per-layer events would break)
+    dense = [i for i, m in enumerate(modes) if m != W.SPARSE]
+    plan_dense = td.Plan(shape, [modes[i] for i in dense], [q[i] for i in dense],
+                         [K[i] for i in dense], [V[i] for i in dense], seq, wl.top_k, idx,
+                         [outs[i] for i in dense], None, ws)
     # the same PPSA step with the new token's K/V rows appended to every layer's
     # cache by the attention kernels themselves (rewrites position N_b - 1)
     gen = torch.Generator(device=device).manual_seed(wl.seed + 77)
@@ -373,6 +413,8 @@ def run_ours(args, world, rank, local):
         plan_sel.launch(stream)
         flush_l2()
         plan_app.launch(stream)
+        flush_l2()
+        plan_dense.launch(stream)
         td.td_decode_step(shape, modes, q, K, V, seq, wl.top_k, idx, outs, None, ws,
                           stream=stream)
     torch.cuda.synchronize(device)
@@ -381,6 +423,7 @@ def run_ours(args, world, rank, local):
     with ClockSampler(local) as clocks:
         dist_barrier(world, device)
         torch.cuda.synchronize(device)
+        clocks.mark_start()
         t_wall = time.perf_counter()
         ev_ppsa = graph_pass(plan, K_steps)
         torch.cuda.synchronize(device)
@@ -393,6 +436,9 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(device)
         dist_barrier(world, device)
         ev_app = graph_pass(plan_app, K_steps)
+        torch.cuda.synchronize(device)
+        dist_barrier(world, device)
+        ev_dense = graph_pass(plan_dense, K_steps)
         torch.cuda.synchronize(device)
         dist_barrier(world, device)
         # pass 2: per-layer events around each layer's launches
@@ -417,11 +463,13 @@ def run_ours(args, world, rank, local):
             e[wl.layers].record(stream)
             probe.append(e)
         torch.cuda.synchronize(device)
+        clocks.mark_stop()
         dist_barrier(world, device)
     ppsa_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_ppsa) * 1e3
     full_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_full) * 1e3
     sel_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_sel) * 1e3
     app_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_app) * 1e3
+    dense_us = statistics.fmean(a.elapsed_time(b) for a, b in ev_dense) * 1e3
     per_layer = np.array([[e[i].elapsed_time(e[i + 1]) * 1e3 for i in range(wl.layers)]
                           for e in traced])                      # [K, L] us
     traced_step_us = float(np.mean([e[0].elapsed_time(e[-1]) * 1e3 for e in traced]))
@@ -438,6 +486,7 @@ def run_ours(args, world, rank, local):
     full_us = dist_max(full_us, world, device)
     sel_us = dist_max(sel_us, world, device)
     app_us = dist_max(app_us, world, device)
+    dense_us = dist_max(dense_us, world, device)
 
     # Figure 4(a)'s measure on this data (untimed): the top-k set each layer
     # would select, and its overlap with the next layer's
@@ -482,14 +531,19 @@ def run_ours(args, world, rank, local):
     step_sum = sum(by_mode[k] * counts[k] for k in by_mode)
     kernels = {}
     full_launch_us = by_mode.get("full", by_mode.get("full_select"))
+    tensor = wl.group in (4, 8)  # grouped-query layers run on the tensor-core kernels
     kernels["full"] = {
-        "kernel": "attention_kernel<G,full> (split-K flash decode over all N_b tokens + combine)",
+        "kernel": ("attention_mma16_kernel<G,full> (tensor cores, 16 tokens per warp; "
+                   if tensor else "attention_kernel<G,full> (CUDA cores; ")
+                  + "split-K flash decode over all N_b tokens + combine)",
         "launch_us": full_launch_us, "bytes": bytes_model["per_launch"]["full"],
         "floor_us": floor_by_mode.get("full", floor_by_mode.get("full_select")),
         "share": (full_launch_us * (counts["full"] + counts["full_select"])) / step_sum}
     if "sparse" in by_mode:
         kernels["sparse"] = {
-            "kernel": "attention_kernel<G,sparse> (gather of the k persisted K/V rows + combine)",
+            "kernel": ("attention_mma_kernel<G,sparse> (tensor cores, 8 tokens per warp; "
+                       if tensor else "attention_kernel<G,sparse> (CUDA cores; ")
+                      + "gather of the k persisted K/V rows + combine)",
             "launch_us": by_mode["sparse"], "bytes": bytes_model["per_launch"]["sparse"],
             "floor_us": floor_by_mode["sparse"],
             "share": by_mode["sparse"] * counts["sparse"] / step_sum}
@@ -508,6 +562,20 @@ def run_ours(args, world, rank, local):
     dominant = max(kernels, key=lambda k: kernels[k]["share"])
     sparse_gbs = rooflines["sparse"]["achieved"] if "sparse" in rooflines else None
     launches_per_step = sum(2 if m == W.FULL_SELECT else 1 for m in modes)
+    # the sparse layers inside the graph step: PPSA step minus the same step
+    # without them, against the K/V bytes they read
+    n_sparse = counts["sparse"]
+    sparse_phase = None
+    if n_sparse:
+        phase_us = ppsa_us - dense_us
+        phase_gbs = n_sparse * bytes_model["per_launch"]["sparse"] / (phase_us * 1e-6) / 1e9
+        sparse_phase = {
+            "dense_step_us": round(dense_us, 2), "sparse_layers": n_sparse,
+            "phase_us": round(phase_us, 2), "per_layer_us": round(phase_us / n_sparse, 2),
+            "achieved": round(phase_gbs, 1), "unit": "GB/s", "frac": round(phase_gbs / peak, 4),
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "what": "graph step minus the same graph without its sparse layers; bytes = the "
+                    "sparse layers' algorithmic bytes (K/V rows, indices, q, out)"}
 
     result = None
     if rank == 0:
@@ -548,6 +616,7 @@ def run_ours(args, world, rank, local):
             "traced_step_us": round(traced_step_us, 2),
             "layer_us": {k: round(v, 2) for k, v in by_mode.items()},
             "sparse_layer_gbs": round(sparse_gbs, 1) if sparse_gbs else None,
+            "sparse_phase_in_graph": sparse_phase,
             "roofline": rooflines[dominant],
             "rooflines": rooflines,
             "gpu_launches": launches_per_step * K_steps,
@@ -567,7 +636,8 @@ def run_ours(args, world, rank, local):
             reps += 1
         per_step_us = secs / reps * (groups / len(pick)) * 1e6
         result["cpu_baseline"] = {
-            "value": round(per_step_us, 1), "unit": "us", "cores": threads, "kind": "oracle",
+            "value": round(per_step_us, 1), "unit": "us", "cores": min(threads, len(pick)),
+            "kind": "oracle",
             "sample": f"{len(pick)} of {groups} (batch row, KV head) groups through all "
                       f"{wl.layers} layers, x{reps} runs, scaled to the whole step",
         }
@@ -621,7 +691,7 @@ def run_reference(args, world, rank, local):
         "config": {"workload": wl.name, "batch": wl.batch, "layers": wl.layers,
                    "q_heads": wl.q_heads, "kv_heads": wl.kv_heads, "seq_len": wl.max_seq_len,
                    "top_k": wl.top_k, "parallelism": "host cores (oracle)"},
-        "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": threads,
+        "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": min(threads, n_done),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": "us", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

@@ -70,7 +70,8 @@ typedef enum {
 #define TD_FLAG_INDEX_OUT_OF_RANGE 0x1u   /* idx entry < -1 or >= seq_lens[b]: skipped */
 #define TD_FLAG_SEQ_LEN_OUT_OF_RANGE 0x2u /* seq_lens[b] < 0 or > max_seq_len: clamped */
 #define TD_FLAG_WAIT_TIMEOUT 0x4u         /* a staged kernel's bounded wait for its copies gave up;
-                                             that (batch, KV head)'s output is not written */
+                                             that (batch, KV head)'s output lacks the tokens of
+                                             the CTA that gave up (the workspace stays usable) */
 
 typedef struct {
     int32_t batch;          /* B  >= 1                                         */
@@ -192,7 +193,12 @@ td_status td_sparse_attn(const td_shape *shape, const void *q, const void *k_cac
 /*
  * td_sparse_attn for callers that cannot allocate device memory.  The paper
  * has no counterpart: this is a deployment variant of the PPSA layer above,
- * with the same arguments minus the workspace and the same result.
+ * with the same arguments minus the workspace.  It runs the kernel
+ * td_sparse_attn runs by default (tensor cores for G = 4, 8; CUDA cores
+ * otherwise) with a split plan of its own (about 256 index entries per CTA,
+ * fewer splits when the scratch would not hold their partials), so its
+ * result agrees with td_sparse_attn's within the parity tolerance (bf16
+ * max-abs 2e-2, fp32 row-relative 1e-5), not bit for bit.
  *
  * Who needs it: code that may not call cudaMalloc or own a workspace -- a
  * component inside a host framework that hands out all device memory from
@@ -203,14 +209,19 @@ td_status td_sparse_attn(const td_shape *shape, const void *q, const void *k_cac
  * TD_NOALLOC_SCRATCH_BYTES bytes inside the library's device image, which
  * every GPU that loads the library keeps until the process exits.
  *   - The first call on a device looks up the array's address (per device,
- *     with that device current); make that first call before any stream
- *     capture starts.
+ *     with that device current) and caches it for the CUDA context current
+ *     then; a later call in another context (after cudaDeviceReset, say)
+ *     looks it up again.  Make the first call in each context before any
+ *     stream capture starts.
  *   - Every call shares the array, which keeps the last call's contents; each
  *     call clears the parts that must start at zero on its own stream.  Calls
  *     whose kernels overlap on the GPU race on the array: keep them ordered on
  *     one stream.
  *   - Shapes whose scratch would exceed the array return
- *     TD_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *     TD_ERR_WORKSPACE_TOO_SMALL before anything is launched.  A shape whose
+ *     top_k fits one CTA (at most 2048 entries) needs only the tickets and the
+ *     status word (4 bytes per (batch row, KV head)); more splits add
+ *     (2 + 128) * 4 bytes per split and query head.
  *   - Out-of-range index entries are skipped as in td_sparse_attn; this entry
  *     point does not report the status word.
  */
@@ -348,6 +359,21 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *                   CTAs per SM); other values restore the default
  *   "pdl", "topk_pdl": 0 turns off programmatic dependent launch between a
  *                   call's kernels / before the top-k kernel (default 1)
+ *   "mma_full_tokens", "mma_sparse_tokens": tokens each warp of a
+ *          tensor-core full (and full+select) / sparse kernel takes per round:
+ *          8 (CTAs of 8 warps) or 16 (CTAs of 4 warps, both row groups of the
+ *          MMA); defaults 16 for full layers, 8 for sparse layers; other
+ *          values restore the default
+ *   "wait_limit_us": microseconds after which a staged full-layer CTA stops
+ *          waiting for a bulk copy (default 1 s).  A CTA that gives up waits
+ *          (at the default limit) for every copy it issued, then joins the
+ *          split merge with an empty partial and sets TD_FLAG_WAIT_TIMEOUT:
+ *          the layer's output lacks that CTA's tokens and the workspace stays
+ *          consistent for the next launch
+ *   "wait_test": 1 makes the first stage wait of every staged full-layer CTA
+ *          poll a barrier that nothing arrives on, so it runs out after
+ *          "wait_limit_us" (tests of the failure report; no fault, no hang);
+ *          0 (default) in normal use
  * Otherwise value <= 0 restores the default.  Unknown key -> TD_ERR_INVALID_ARG.
  */
 td_status td_set_tuning(const char *key, int32_t value);

@@ -13,6 +13,7 @@ MODE_SPARSE = 2
 FLAG_INDEX_OUT_OF_RANGE = 0x1
 FLAG_SEQ_LEN_OUT_OF_RANGE = 0x2
 FLAG_WAIT_TIMEOUT = 0x4
+NOALLOC_SCRATCH_BYTES = 8 << 20  # TD_NOALLOC_SCRATCH_BYTES: td_sparse_attn_noalloc's fixed scratch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 

@@ -40,6 +40,12 @@ struct Tuning {
     int topk_warp_max = 0;       // top-k threshold bins up to this size finish in one warp (0: 256)
     int pdl = 1;                 // 0: no programmatic dependent launch between a call's kernels
     int topk_pdl = 1;            // 0: the top-k kernel waits for its attention kernel in stream order
+    int mma_full_tokens = 16;    // tensor-core full / full+select kernels: tokens per warp per round
+    int mma_sparse_tokens = 8;   // tensor-core sparse kernels: tokens per warp per round (8 or 16)
+    int wait_limit_us = 0;       // staged full layers: microseconds a stage wait may take before it
+                                 // gives up and the launch reports TD_FLAG_WAIT_TIMEOUT (0: 1 s)
+    int wait_test = 0;           // 1: each staged full-layer CTA's first wait polls a barrier that
+                                 // nothing arrives on, so it runs out (failure-report tests)
 };
 Tuning g_tuning;
 const Tuning kDefaultTuning;
@@ -50,12 +56,20 @@ const Tuning kDefaultTuning;
 // full layers and match the CUDA-core ones on sparse layers.
 bool mma_for(int G) { return g_tuning.mma != 0 && td::mma_supported(G); }
 
+// Measured on GB300: the 16-token tensor-core kernel (CTAs of 4 warps, both
+// MMA row groups) takes 2-6% off full and full+select layers; on sparse
+// layers it is 9-30% slower than the 8-token kernel, which stays there.
 // Measured on GB300: prefetching the next round's K/V lines into L2 takes
 // 10% off the tensor-core full layers (32K, G = 4) and costs 5% on the MHA
 // full layers at 10K.
 int prefetch_for(int G)
 {
     return g_tuning.full_prefetch < 0 ? (mma_for(G) ? 1 : 0) : g_tuning.full_prefetch;
+}
+
+int mma_tokens_for(bool sparse)
+{
+    return sparse ? g_tuning.mma_sparse_tokens : g_tuning.mma_full_tokens;
 }
 
 bool staged_for(bool sparse, int G)
@@ -205,7 +219,7 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
     const long units = (long)s.batch * s.num_kv_heads;
     int per_sm = sparse ? g_tuning.sparse_ctas_per_sm : g_tuning.full_ctas_per_sm;
     if (per_sm <= 0)
-        per_sm = mma_for(G) ? td::attention_mma_ctas_per_sm(G, sparse, select)
+        per_sm = mma_for(G) ? td::attention_mma_ctas_per_sm(G, sparse, select, mma_tokens_for(sparse))
                             : td::attention_ctas_per_sm(G, sparse, select, staged_for(sparse, G));
     const long slots = (long)device_sm_count() * per_sm;  // resident CTAs per wave
     int waves = sparse ? g_tuning.sparse_waves : g_tuning.full_waves;
@@ -277,6 +291,8 @@ td::AttnArgs base_args(const Ctx &c, const void *q, const void *k, const void *v
     a.Hkv = c.shape.num_kv_heads;
     a.Nmax = c.shape.max_seq_len;
     a.scale = c.scale;
+    a.wait_limit_us = g_tuning.wait_limit_us;
+    a.wait_test = g_tuning.wait_test;
     return a;
 }
 
@@ -315,7 +331,8 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
     plan_splits(c.shape, c.shape.max_seq_len, false, select, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
     const cudaError_t le =
-        mma_for(c.G) ? td::launch_attention_mma(c.G, false, select, a, c.shape.batch, pdl, st)
+        mma_for(c.G) ? td::launch_attention_mma(c.G, false, select, mma_tokens_for(false), a,
+                                                c.shape.batch, pdl, st)
                      : td::launch_attention(c.G, false, select, cluster, staged_for(false, c.G), a,
                                             c.shape.batch, pdl, st);
     if (le != cudaSuccess)
@@ -368,7 +385,8 @@ td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
     plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
     const cudaError_t le =
-        mma_for(c.G) ? td::launch_attention_mma(c.G, true, false, a, c.shape.batch, pdl, st)
+        mma_for(c.G) ? td::launch_attention_mma(c.G, true, false, mma_tokens_for(true), a,
+                                                c.shape.batch, pdl, st)
                      : td::launch_attention(c.G, true, false, cluster, staged_for(true, c.G), a,
                                             c.shape.batch, pdl, st);
     if (le != cudaSuccess)
@@ -826,6 +844,15 @@ td_status td_set_tuning(const char *key, int32_t value)
         g_tuning.pdl = value != 0 ? 1 : 0;
     else if (!strcmp(key, "topk_pdl"))
         g_tuning.topk_pdl = value != 0 ? 1 : 0;
+    else if (!strcmp(key, "mma_full_tokens"))
+        g_tuning.mma_full_tokens = (value == 8 || value == 16) ? value : kDefaultTuning.mma_full_tokens;
+    else if (!strcmp(key, "mma_sparse_tokens"))
+        g_tuning.mma_sparse_tokens =
+            (value == 8 || value == 16) ? value : kDefaultTuning.mma_sparse_tokens;
+    else if (!strcmp(key, "wait_limit_us"))
+        g_tuning.wait_limit_us = value > 0 ? value : kDefaultTuning.wait_limit_us;
+    else if (!strcmp(key, "wait_test"))
+        g_tuning.wait_test = value > 0 ? 1 : 0;
     else if (!strcmp(key, "topk_threads"))
         g_tuning.topk_threads = (value == 512 || value == 1024) ? value : 0;
     else if (!strcmp(key, "attn_carveout"))

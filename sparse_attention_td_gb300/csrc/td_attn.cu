@@ -40,7 +40,7 @@ namespace {
 constexpr int kStageRowBytes = kHeadDim * 2;                   // one bf16 row
 constexpr int kStageBytes = 2 * kTokPerRound * kStageRowBytes;  // K block + V block = 32 KB
 constexpr int kStageTxPerToken = 2 * kStageRowBytes;
-constexpr long kSpinLimit = 1L << 22;  // bounded mbarrier wait (try_wait suspends between polls)
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded mbarrier wait gives up after 1 s
 
 // Ring depth per group size: two CTAs per SM where registers allow it.
 __host__ __device__ constexpr int staged_stages(int G)
@@ -67,11 +67,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned by
                  : "memory");
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity)
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase with the given parity to complete: polls until
+// it has, or until `limit_ns` nanoseconds of the global timer have passed
+// (then false).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     const uint32_t addr = smem_u32(bar);
-    for (long i = 0; i < kSpinLimit; ++i) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
@@ -82,8 +93,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity)
             : "memory");
         if (done)
             return true;
+        if (global_ns() - t0 > limit_ns)
+            return false;
     }
-    return false;
 }
 
 // Global -> shared bulk copy (16-byte aligned addresses, size a multiple of
@@ -138,6 +150,9 @@ attention_kernel(const AttnArgs a)
     constexpr int S = staged_stages(G);
     extern __shared__ __align__(128) unsigned char sm_stage[];  // STAGED: [S][K rows | V rows]
     __shared__ __align__(8) uint64_t sm_full[STAGED ? S : 1];
+    // a barrier nothing ever arrives on: with a.wait_test set, each CTA's
+    // first stage wait polls it, so that the wait runs out (failure-report tests)
+    __shared__ __align__(8) uint64_t sm_never;
     __shared__ float sm_m[kAttnWarps][G];
     __shared__ float sm_l[kAttnWarps][G];
     __shared__ float sm_w[kAttnWarps][G];
@@ -276,6 +291,7 @@ attention_kernel(const AttnArgs a)
         if (tid == 0) {
             for (int i = 0; i < S; ++i)
                 mbar_init(&sm_full[i], 1);
+            mbar_init(&sm_never, 1);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
         __syncthreads();
@@ -446,10 +462,15 @@ attention_kernel(const AttnArgs a)
     } else if constexpr (STAGED) {
         int it = 0;
         bool failed = false;
+        const uint64_t limit = a.wait_limit_us > 0 ? (uint64_t)a.wait_limit_us * 1000ull
+                                                    : kWaitLimitNs;
         for (; it < n_it; ++it) {
             const int st = it % S;
-            // false only if a copy never completed: reported, the CTA stops below
-            const bool landed = mbar_wait(&sm_full[st], (unsigned)(it / S) & 1u);
+            // false only if a copy did not complete within the limit:
+            // reported, and the CTA's partial is discarded below
+            const bool landed =
+                (a.wait_test && it == 0) ? mbar_wait(&sm_never, 0u, limit)
+                                         : mbar_wait(&sm_full[st], (unsigned)(it / S) & 1u, limit);
             const unsigned char *kst = sm_stage + st * kStageBytes;
             const unsigned char *vst = kst + kStageBytes / 2;
             const int base = t0 + it * kTokPerRound;
@@ -476,13 +497,28 @@ attention_kernel(const AttnArgs a)
             }
         }
         if (failed) {
-            // stages still in flight land before the CTA exits (bounded), then report
+            // Every stage issued and not yet consumed (the one that did not
+            // land, and those after it) lands before the CTA goes on: one
+            // bounded wait each at the default limit, so no copy into this CTA's
+            // shared memory is in flight when it exits.  Then the CTA takes
+            // part in the split merge with an empty partial (m = -inf, l = 0),
+            // so the (batch row, KV head)'s merge still runs and its ticket
+            // returns to zero for the next launch on this workspace; the
+            // output misses this split's tokens and the status word says so.
             if (tid == 0) {
-                for (int j = it + 1; j < n_it && j < it + S; ++j)
+                for (int j = it; j < n_it && j < it + S; ++j)
                     mbar_wait(&sm_full[j % S], (unsigned)(j / S) & 1u);
                 atomicOr(a.status, kFlagWaitTimeout);
             }
-            return;
+            __syncthreads();
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                m[h] = -CUDART_INF_F;
+                l[h] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    o[h][j] = make_float2(0.0f, 0.0f);
+            }
         }
     } else {
         if (t0 < t1)

@@ -97,8 +97,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f)
 // sm_w[w][h] towards the CTA's running maximum sm_M[h] (log2 units) and
 // denominator sm_L[h].  One split: write the normalised output.  Several:
 // publish this split's partial and let the last CTA to arrive merge them all.
-// All threads of the CTA call it.
-template <int G>
+// All NT threads (NW warps) of the CTA call it.
+template <int G, int NW = kAttnWarps, int NT = kAttnThreads>
 __device__ __forceinline__ void finish_splits(const AttnArgs &a, const float (*sm_o)[G][kHeadDim],
                                               const float (*sm_w)[G], const float *sm_M,
                                               const float *sm_L, int *sm_last, size_t bg,
@@ -106,11 +106,11 @@ __device__ __forceinline__ void finish_splits(const AttnArgs &a, const float (*s
 {
     const int tid = threadIdx.x;
     if (nsplit_b == 1) {
-        for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
+        for (int e = tid; e < G * kHeadDim; e += NT) {
             const int h = e / kHeadDim, d = e % kHeadDim;
             float acc = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w)
+            for (int w = 0; w < NW; ++w)
                 acc += sm_o[w][h][d] * sm_w[w][h];
             const float L = sm_L[h];
             const float val = L > 0.0f ? acc / L : 0.0f;
@@ -123,11 +123,11 @@ __device__ __forceinline__ void finish_splits(const AttnArgs &a, const float (*s
 
     // Several splits: publish this split's partial result.
     const size_t pbase = (bg * (size_t)a.nsplit + split) * G;
-    for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
+    for (int e = tid; e < G * kHeadDim; e += NT) {
         const int h = e / kHeadDim, d = e % kHeadDim;
         float acc = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w)
+        for (int w = 0; w < NW; ++w)
             acc += sm_o[w][h][d] * sm_w[w][h];
         a.part_o[(pbase + h) * kHeadDim + d] = acc;
     }
@@ -158,7 +158,7 @@ __device__ __forceinline__ void finish_splits(const AttnArgs &a, const float (*s
     // then reduces locally: one round trip instead of three with barriers.
     const size_t pb0 = bg * (size_t)a.nsplit * G;
     constexpr int kMergeChunk = 16;
-    for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
+    for (int e = tid; e < G * kHeadDim; e += NT) {
         const int h = e / kHeadDim, d = e % kHeadDim;
         float M = -CUDART_INF_F, L = 0.0f, acc = 0.0f;
         for (int s0 = 0; s0 < nsplit_b; s0 += kMergeChunk) {

@@ -6,8 +6,18 @@
 // query heads done by mma.sync m16n8k16 (bf16 inputs, fp32 accumulation):
 //   S[token][head] = K Q^T   (M = tokens, N = heads padded to 8, K = dims)
 //   O[dim][head]  += V^T P^T (M = dims,   N = heads,              K = tokens)
-// A warp takes 8 tokens per round (the upper 8 MMA rows stay zero), a CTA of
-// 8 warps 64, as in the CUDA-core kernels, and the splits merge the same way.
+// Two kernels, the same arithmetic, different tiling:
+//   * attention_mma_kernel: a warp takes 8 tokens per round (MMA rows 8..15
+//     of S and tokens 8..15 of the P V k-step stay zero), a CTA of 8 warps
+//     64 tokens; 2 CTAs per SM.  Default for sparse layers.
+//   * attention_mma16_kernel: a warp takes 16 tokens per round (rows r and
+//     r + 8 of S are two tokens, the P V k-step takes all 16), a CTA of 4
+//     warps 64 tokens; half the MMAs and shuffles per token, 3 CTAs per SM.
+//     Default for full and full+select layers.
+// Measured on GB300 (design notes): the 16-token kernel takes 2-6% off full
+// and full+select layers, but is slower on sparse layers, whose CTAs are
+// short and latency-bound; there the 8-token kernel stays.  The splits of
+// either merge as in the CUDA-core kernels.
 //
 // Fragments come straight from global memory.  The dot product does not care
 // in which order the 128 dims are summed, so k-step j of the S product maps
@@ -316,64 +326,357 @@ attention_mma_kernel(const AttnArgs a)
     finish_splits<G>(a, sm_o, sm_w, sm_M, sm_L, &sm_last, bg, split, nsplit_b, out_row0);
 }
 
+// 16 tokens per warp per round, CTAs of 4 warps (kTokPerRound tokens a CTA
+// round), at most 168 registers for 3 CTAs per SM.  Fragment maps as in
+// attention_mma_kernel, with the MMAs' second row group filled: K of tokens
+// r and r + 8 (A rows r, r + 8 of S); V of tokens 2c, 2c+1, 2c+8, 2c+9 (the
+// P V k-step's 16 tokens); P of the same four tokens per head.
+constexpr int kMma16Warps = kTokPerRound / 16;
+constexpr int kMma16Threads = kMma16Warps * 32;
+
 template <int G, bool SPARSE, bool SELECT>
-cudaError_t launch_mma_one(const AttnArgs &a, int batch, bool pdl, cudaStream_t stream)
+__global__ void __launch_bounds__(kMma16Threads, 3)
+attention_mma16_kernel(const AttnArgs a)
+{
+    static_assert(G == 4 || G == 8, "heads of a group are the MMA's N = 8 columns");
+    constexpr int NW = kMma16Warps, NT = kMma16Threads;
+    __shared__ float sm_m[NW][G];
+    __shared__ float sm_l[NW][G];
+    __shared__ float sm_w[NW][G];
+    __shared__ __align__(16) float sm_o[NW][G][kHeadDim];
+    __shared__ float sm_M[G];
+    __shared__ float sm_L[G];
+    __shared__ int sm_rows[SPARSE ? kMaxSparseChunk : 1];
+    __shared__ int sm_last;
+    __shared__ unsigned sm_hist[SELECT ? kSelectBins : 1];
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = lane >> 2, c = lane & 3;  // MMA fragment row group / quad position
+
+    int n_b = a.seq_lens[b];
+    if (n_b < 0 || n_b > a.Nmax) {
+        if (tid == 0)
+            atomicOr(a.status, kFlagSeqLenOutOfRange);
+        n_b = n_b < 0 ? 0 : a.Nmax;
+    }
+    const int n_total = SPARSE ? a.top_k : n_b;
+    const int nsplit_b = n_total > 0 ? (n_total + a.chunk - 1) / a.chunk : 1;
+    if (split >= nsplit_b)
+        return;
+    const int t0 = split * a.chunk;
+    const int t1 = min(t0 + a.chunk, n_total);
+    const size_t bg = (size_t)b * a.Hkv + g;
+    const uint16_t *kbase = a.k + bg * (size_t)a.Nmax * kHeadDim;
+    const uint16_t *vbase = a.v + bg * (size_t)a.Nmax * kHeadDim;
+
+    if constexpr (SELECT) {
+        for (int i = tid; i < kSelectBins; i += NT)
+            sm_hist[i] = 0u;
+        __syncthreads();
+    }
+    if constexpr (SPARSE) {
+        if (a.idx_dep)
+            pdl_wait();
+        const int32_t *ip = a.idx + bg * (size_t)a.top_k;
+        for (int j = tid; j < t1 - t0; j += NT) {
+            int rr = ip[t0 + j];
+            if (rr < -1 || rr >= n_b) {
+                atomicOr(a.status, kFlagIndexOutOfRange);
+                rr = -1;
+            }
+            sm_rows[j] = rr;
+        }
+        __syncthreads();
+    }
+    auto row_of = [&](int t) { return t < t1 ? (SPARSE ? sm_rows[t - t0] : t) : -1; };
+
+    // This warp's 16 tokens of the round at `base`: K of tokens r, r + 8
+    // (dims 16j + 4c .. +3 for k-step j); V of tokens 2c, 2c+1, 2c+8, 2c+9
+    // (dims 8r..8r+7 and 64+8r..64+8r+7).
+    auto load = [&](int base, uint2 (&kq)[2][8], uint4 (&vv)[4][2]) {
+        const int tw = base + warp * 16;
+        const int rk[2] = {row_of(tw + r), row_of(tw + r + 8)};
+        const int rv[4] = {row_of(tw + 2 * c), row_of(tw + 2 * c + 1), row_of(tw + 2 * c + 8),
+                           row_of(tw + 2 * c + 9)};
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                kq[t][j] = rk[t] >= 0 ? ldg8(kbase + (size_t)rk[t] * kHeadDim + 16 * j + 4 * c)
+                                      : make_uint2(0u, 0u);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                vv[t][i] = rv[t] >= 0 ? ldg16(vbase + (size_t)rv[t] * kHeadDim + 64 * i + 8 * r)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+    };
+    // L2 prefetch of this warp's round (two calls of 8 tokens)
+    auto prefetch = [&](int base) {
+        prefetch_round_l2(kbase, vbase, base + warp * 16, lane, row_of);
+        prefetch_round_l2(kbase, vbase, base + warp * 16 + 8, lane, row_of);
+    };
+    uint2 kq0[2][8];
+    uint4 vv0[4][2];
+    load(t0, kq0, vv0);  // the cache is never written by a kernel of the step
+    // full layers: rounds 1 .. prefetch go to L2 now, later rounds `prefetch`
+    // ahead of use
+    const int pf = SPARSE ? 0 : a.prefetch;
+    for (int d = 1; d <= pf; ++d)
+        prefetch(t0 + d * kTokPerRound);
+    pdl_wait();
+
+    // q of head r (heads >= G are zero columns): dims 16j + 4c .. +3.
+    uint2 qf[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        qf[j] = r < G ? *reinterpret_cast<const uint2 *>(
+                            a.q + ((size_t)b * a.Hq + (size_t)g * G + r) * kHeadDim + 16 * j + 4 * c)
+                      : make_uint2(0u, 0u);
+
+    const float c2 = a.scale * kLog2e;
+    float m[2] = {-CUDART_INF_F, -CUDART_INF_F};  // heads 2c, 2c+1 (replicated over r)
+    float l[2] = {0.0f, 0.0f};
+    // m-tile i holds dims vdim(i) (0, 1: heads 2c, 2c+1) and vdim(i) + 1 (2, 3),
+    // vdim(i) = (i < 4 ? 8r : 64 + 8r) + 2 (i % 4)
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[i][j] = 0.0f;
+
+    auto round = [&](int base, const uint2 (&kq)[2][8], const uint4 (&vv)[4][2]) {
+        const int tw = base + warp * 16;
+        // s[0], s[1]: token r, heads 2c, 2c+1; s[2], s[3]: token r + 8
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            mma_bf16(s, kq[0][j].x, kq[1][j].x, kq[0][j].y, kq[1][j].y, qf[j].x, qf[j].y);
+        const bool ok[2] = {row_of(tw + r) >= 0, row_of(tw + r + 8) >= 0};
+
+        if constexpr (SELECT) {
+            // selection scores of tokens tw + r, tw + r + 8: the group's summed
+            // scaled logits (lane c = 0 stores the first, c = 1 the second)
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                float sc = (2 * c < G ? s[2 * t] * a.scale : 0.0f) +
+                           (2 * c + 1 < G ? s[2 * t + 1] * a.scale : 0.0f);
+                sc += __shfl_xor_sync(kFull, sc, 1);
+                sc += __shfl_xor_sync(kFull, sc, 2);
+                const int tok = tw + r + 8 * t;
+                if (c == t && tok < t1) {
+                    a.scores[bg * (size_t)a.Nmax + tok] = sc;
+                    atomicAdd(&sm_hist[order_key(sc) >> (32 - kSelectBits)], 1u);
+                }
+            }
+        }
+
+        // online softmax of heads 2c, 2c+1 over the warp's 16 tokens
+        float p[2][2];  // [head 2c + e][token r, r + 8]
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool head = 2 * c + e < G;
+            const float x0 = (ok[0] && head) ? s[e] * c2 : -CUDART_INF_F;
+            const float x1 = (ok[1] && head) ? s[2 + e] * c2 : -CUDART_INF_F;
+            float mx = fmaxf(x0, x1);
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+            const float m_new = fmaxf(m[e], mx);
+            float alpha = 1.0f;
+            p[e][0] = p[e][1] = 0.0f;
+            if (m_new != -CUDART_INF_F) {  // uniform over the 8 lanes of this head
+                alpha = safe_exp2_diff(m[e], m_new);
+                p[e][0] = (x0 == -CUDART_INF_F) ? 0.0f : exp2f(x0 - m_new);
+                p[e][1] = (x1 == -CUDART_INF_F) ? 0.0f : exp2f(x1 - m_new);
+            }
+            float ps = p[e][0] + p[e][1];
+            ps += __shfl_xor_sync(kFull, ps, 4);
+            ps += __shfl_xor_sync(kFull, ps, 8);
+            ps += __shfl_xor_sync(kFull, ps, 16);
+            if (m_new != -CUDART_INF_F) {
+                l[e] = l[e] * alpha + ps;
+                m[e] = m_new;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    o[i][e] *= alpha;
+                    o[i][e + 2] *= alpha;
+                }
+            }
+        }
+
+        // P^T fragment: P[token 2c + 8t][head r], P[token 2c + 1 + 8t][head r],
+        // held by lanes (row 2c / 2c+1, quad r / 2) in p[r & 1][t]
+        const int src0 = 8 * c + (r >> 1), src1 = 8 * c + 4 + (r >> 1);
+        uint32_t pb[2][3];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const float a0p = __shfl_sync(kFull, p[0][t], src0), a1p = __shfl_sync(kFull, p[1][t], src0);
+            const float b0p = __shfl_sync(kFull, p[0][t], src1), b1p = __shfl_sync(kFull, p[1][t], src1);
+            float pt0 = (r & 1) ? a1p : a0p;
+            float pt1 = (r & 1) ? b1p : b0p;
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {  // p = p1 + p2 + p3 in bf16
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(pt0), h1 = __float2bfloat16_rn(pt1);
+                pb[t][k] =
+                    (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                pt0 -= __bfloat162float(h0);
+                pt1 -= __bfloat162float(h1);
+            }
+        }
+        // O += V^T P^T, one m-tile of 16 dims at a time, k = tokens 2c, 2c+1,
+        // 2c+8, 2c+9
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w0 = word2(vv[0], i), w1 = word2(vv[1], i);
+            const uint32_t w8 = word2(vv[2], i), w9 = word2(vv[3], i);
+            const uint32_t lo = prmt(w0, w1, 0x5410u), hi = prmt(w0, w1, 0x7632u);
+            const uint32_t lo8 = prmt(w8, w9, 0x5410u), hi8 = prmt(w8, w9, 0x7632u);
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+                mma_bf16(o[i], lo, hi, lo8, hi8, pb[0][k], pb[1][k]);
+        }
+    };
+
+    if (t0 < t1)
+        round(t0, kq0, vv0);
+    for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
+        uint2 kq[2][8];
+        uint4 vv[4][2];
+        if (pf > 0)
+            prefetch(base + pf * kTokPerRound);
+        load(base, kq, vv);
+        round(base, kq, vv);
+    }
+
+    pdl_launch_dependents();
+
+    // this warp's partial into shared memory (dims back in natural order)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int h = 2 * c + e;
+        if (h < G) {
+            if (r == 0) {
+                sm_m[warp][h] = m[e];
+                sm_l[warp][h] = l[e];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d = (i < 4 ? 8 * r : 64 + 8 * r) + 2 * (i & 3);
+                sm_o[warp][h][d] = o[i][e];
+                sm_o[warp][h][d + 1] = o[i][e + 2];
+            }
+        }
+    }
+    __syncthreads();
+    if constexpr (SELECT) {
+        unsigned *gh = a.hist + bg * kSelectBins;
+        for (int i = tid; i < kSelectBins; i += NT)
+            if (sm_hist[i])
+                atomicAdd(&gh[i], sm_hist[i]);
+    }
+    if (tid < G) {
+        const int h = tid;
+        float M = -CUDART_INF_F;
+        for (int w = 0; w < NW; ++w)
+            M = fmaxf(M, sm_m[w][h]);
+        float L = 0.0f;
+        for (int w = 0; w < NW; ++w) {
+            const float wt = safe_exp2_diff(sm_m[w][h], M);
+            sm_w[w][h] = wt;
+            L += sm_l[w][h] * wt;
+        }
+        sm_M[h] = M;
+        sm_L[h] = L;
+    }
+    __syncthreads();
+    const size_t out_row0 = (size_t)b * a.Hq + (size_t)g * G;
+    finish_splits<G, NW, NT>(a, sm_o, sm_w, sm_M, sm_L, &sm_last, bg, split, nsplit_b, out_row0);
+}
+
+template <typename Kern>
+cudaError_t launch_kernel(Kern kern, int threads, const AttnArgs &a, int batch, bool pdl,
+                          cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.nsplit, (unsigned)a.Hkv, (unsigned)batch);
-    cfg.blockDim = dim3(kAttnThreads);
+    cfg.blockDim = dim3(threads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attention_mma_kernel<G, SPARSE, SELECT>, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int G, bool SPARSE, bool SELECT>
-int mma_occupancy_one()
+template <typename Kern>
+int occupancy(Kern kern, int threads)
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, attention_mma_kernel<G, SPARSE, SELECT>, kAttnThreads, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, 0) != cudaSuccess)
         return 1;
     return n > 0 ? n : 1;
 }
 
+template <int G, bool SPARSE, bool SELECT>
+cudaError_t launch_mma_one(int tokens, const AttnArgs &a, int batch, bool pdl, cudaStream_t st)
+{
+    return tokens == 16
+               ? launch_kernel(attention_mma16_kernel<G, SPARSE, SELECT>, kMma16Threads, a, batch,
+                               pdl, st)
+               : launch_kernel(attention_mma_kernel<G, SPARSE, SELECT>, kAttnThreads, a, batch,
+                               pdl, st);
+}
+
+template <int G, bool SPARSE, bool SELECT>
+int mma_occupancy_one(int tokens)
+{
+    return tokens == 16 ? occupancy(attention_mma16_kernel<G, SPARSE, SELECT>, kMma16Threads)
+                        : occupancy(attention_mma_kernel<G, SPARSE, SELECT>, kAttnThreads);
+}
+
 template <int G>
-cudaError_t launch_mma_g(bool sparse, bool select, const AttnArgs &a, int batch, bool pdl,
-                         cudaStream_t st)
+cudaError_t launch_mma_g(bool sparse, bool select, int tokens, const AttnArgs &a, int batch,
+                         bool pdl, cudaStream_t st)
 {
     if (sparse)
-        return launch_mma_one<G, true, false>(a, batch, pdl, st);
+        return launch_mma_one<G, true, false>(tokens, a, batch, pdl, st);
     if (select)
-        return launch_mma_one<G, false, true>(a, batch, pdl, st);
-    return launch_mma_one<G, false, false>(a, batch, pdl, st);
+        return launch_mma_one<G, false, true>(tokens, a, batch, pdl, st);
+    return launch_mma_one<G, false, false>(tokens, a, batch, pdl, st);
+}
+
+template <int G>
+int mma_occupancy_g(bool sparse, bool select, int tokens)
+{
+    return sparse ? mma_occupancy_one<G, true, false>(tokens)
+                  : (select ? mma_occupancy_one<G, false, true>(tokens)
+                            : mma_occupancy_one<G, false, false>(tokens));
 }
 
 }  // namespace
 
 bool mma_supported(int G) { return G == 4 || G == 8; }
 
-cudaError_t launch_attention_mma(int G, bool sparse, bool select, const AttnArgs &a, int batch,
-                                 bool pdl, cudaStream_t stream)
+cudaError_t launch_attention_mma(int G, bool sparse, bool select, int tokens, const AttnArgs &a,
+                                 int batch, bool pdl, cudaStream_t stream)
 {
     if (G == 4)
-        return launch_mma_g<4>(sparse, select, a, batch, pdl, stream);
+        return launch_mma_g<4>(sparse, select, tokens, a, batch, pdl, stream);
     if (G == 8)
-        return launch_mma_g<8>(sparse, select, a, batch, pdl, stream);
+        return launch_mma_g<8>(sparse, select, tokens, a, batch, pdl, stream);
     return cudaErrorInvalidValue;
 }
 
-int attention_mma_ctas_per_sm(int G, bool sparse, bool select)
+int attention_mma_ctas_per_sm(int G, bool sparse, bool select, int tokens)
 {
     if (G == 4)
-        return sparse ? mma_occupancy_one<4, true, false>()
-                      : (select ? mma_occupancy_one<4, false, true>() : mma_occupancy_one<4, false, false>());
+        return mma_occupancy_g<4>(sparse, select, tokens);
     if (G == 8)
-        return sparse ? mma_occupancy_one<8, true, false>()
-                      : (select ? mma_occupancy_one<8, false, true>() : mma_occupancy_one<8, false, false>());
+        return mma_occupancy_g<8>(sparse, select, tokens);
     return 1;
 }
 

@@ -51,6 +51,9 @@ struct AttnArgs {
     int chunk;               // tokens (full) or index entries (sparse) per split
     int nsplit;              // gridDim.x
     int prefetch;            // full layers: rounds ahead whose rows each warp prefetches into L2 (0: none)
+    int wait_limit_us;       // staged full layers: microseconds before a stage wait gives up (0: 1 s)
+    int wait_test;           // staged full layers: each CTA's first wait polls a barrier nothing
+                             // arrives on (tests of the failure report); 0 in normal use
     float scale;             // softmax scale (natural-log units)
 };
 
@@ -126,11 +129,12 @@ cudaError_t launch_probe_reads(const ProbeArgs &a, int batch, cudaStream_t strea
 
 // Tensor-core attention (mma.sync over a KV head's G query heads) for
 // G = 4 and 8: same arguments and results as launch_attention (no cluster
-// merge, register-fed fragments).
+// merge, register-fed fragments).  tokens: tokens a warp takes per round,
+// 8 (CTAs of 8 warps) or 16 (CTAs of 4 warps).
 bool mma_supported(int G);
-cudaError_t launch_attention_mma(int G, bool sparse, bool select, const AttnArgs &a, int batch,
-                                 bool pdl, cudaStream_t stream);
-int attention_mma_ctas_per_sm(int G, bool sparse, bool select);
+cudaError_t launch_attention_mma(int G, bool sparse, bool select, int tokens, const AttnArgs &a,
+                                 int batch, bool pdl, cudaStream_t stream);
+int attention_mma_ctas_per_sm(int G, bool sparse, bool select, int tokens);
 
 // Preferred shared-memory carveout (percent, -1 = driver default) for later attention launches.
 void set_attention_carveout(int percent);

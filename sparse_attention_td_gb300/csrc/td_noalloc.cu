@@ -13,7 +13,10 @@
 //
 // Set-up: the first call on a device (with that device current) looks the
 // array's device address up with cudaGetSymbolAddress and caches it per
-// device.  Make that first call before any stream capture begins.
+// device, keyed on the CUDA context current at the time: a call that finds
+// another context current (after cudaDeviceReset, or a driver-API context of
+// the caller's) looks the address up again.  Make the first call in each
+// context before any stream capture begins.
 // Every call shares the one array per device, and it keeps what the last call
 // left there: each call clears the tickets and status word (cudaMemsetAsync on
 // its stream) before its kernel runs.  Calls whose kernels overlap on the GPU
@@ -36,27 +39,61 @@ constexpr size_t kNaAlign = 256;
 constexpr int kMaxDevices = 64;
 constexpr int kEntriesPerCta = 256;  // target index entries per CTA
 constexpr int kMaxNoallocSplits = 64;
+constexpr int kMmaSparseTokens = 8;  // tensor-core sparse kernel variant (tokens per warp per round)
 
 inline size_t na_align(size_t x) { return (x + kNaAlign - 1) & ~(kNaAlign - 1); }
 inline bool na_aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 std::mutex g_mu;
-void *g_scratch[kMaxDevices] = {nullptr};
+struct ScratchAddr {
+    void *ctx;   // context the address was looked up in
+    void *addr;  // device address of g_noalloc_scratch there
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (cached).
+// cuCtxGetCurrent, reached through the runtime (the library does not link the
+// driver library itself); null if the driver does not provide it.
+typedef int (*CtxGetCurrentFn)(void **);
+CtxGetCurrentFn ctx_get_current()
+{
+    static CtxGetCurrentFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return (CtxGetCurrentFn)p;
+    }();
+    return fn;
+}
+
+void *current_ctx()
+{
+    void *ctx = nullptr;
+    if (CtxGetCurrentFn fn = ctx_get_current())
+        if (fn(&ctx) != 0)
+            ctx = nullptr;
+    return ctx;
+}
+
+// Device address of the scratch array in the current context (cached per
+// device and context).
 td_status scratch_address(void **out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return TD_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch[dev]) {
+    void *ctx = current_ctx();
+    if (!g_scratch[dev].addr || !ctx || g_scratch[dev].ctx != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
             return TD_ERR_CUDA;
-        g_scratch[dev] = p;
+        g_scratch[dev].addr = p;
+        g_scratch[dev].ctx = current_ctx();  // current now, if it was not before the lookup
     }
-    *out = g_scratch[dev];
+    *out = g_scratch[dev].addr;
     return TD_OK;
 }
 
@@ -64,6 +101,8 @@ struct NaLayout {
     size_t status, tickets, part_m, part_l, part_o, total;
 };
 
+// With one split a CTA writes its (batch row, KV head)'s output itself, so
+// the layout holds no partials then.
 NaLayout na_layout(size_t units, int nsplit, int G)
 {
     NaLayout L{};
@@ -72,7 +111,7 @@ NaLayout na_layout(size_t units, int nsplit, int G)
     off = na_align(off + sizeof(uint32_t));
     L.tickets = off;
     off = na_align(off + units * sizeof(uint32_t));
-    const size_t slots = units * (size_t)nsplit * (size_t)G;
+    const size_t slots = nsplit > 1 ? units * (size_t)nsplit * (size_t)G : 0;
     L.part_m = off;
     off = na_align(off + slots * sizeof(float));
     L.part_l = off;
@@ -159,7 +198,13 @@ extern "C" td_status td_sparse_attn_noalloc(const td_shape *shape, const void *q
     a.chunk = chunk;
     a.nsplit = nsplit;
     a.scale = s.scale != 0.0f ? s.scale : 1.0f / sqrtf((float)s.head_dim);
-    if (td::launch_attention(G, true, false, false, false, a, s.batch, false, cs) != cudaSuccess)
+    // the kernel td_sparse_attn takes by default: tensor cores for G = 4, 8
+    const cudaError_t le =
+        td::mma_supported(G) ? td::launch_attention_mma(G, true, false, kMmaSparseTokens, a, s.batch,
+                                                        false, cs)
+                             : td::launch_attention(G, true, false, false, false, a, s.batch,
+                                                    false, cs);
+    if (le != cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }

@@ -33,9 +33,11 @@ PATHS = {
     "streamed": {"full_staged": 0, "sparse_staged": 0, "mma": 0},
     "staged": {"full_staged": 1, "sparse_staged": 1, "mma": 0},
     "mma": {"mma": 1},
-    "prefetch2": {"mma": 1, "full_prefetch": 2},
+    "mma8": {"mma": 1, "mma_full_tokens": 8, "full_prefetch": 2},
+    "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},
 }
-TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch")
+TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch", "mma_full_tokens",
+               "mma_sparse_tokens")
 
 
 @pytest.fixture(params=list(PATHS))

@@ -27,12 +27,17 @@ def test_step_bytes_model():
 
 def test_clock_summary_parses_nvidia_smi_rows():
     c = bench.ClockSampler(0)
-    c.lines = ["0, 1965, 2070, 800.1, 0x0, Not Active, Not Active, Not Active, Not Active",
-               "0, 1980, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active",
-               "garbage"]
+    c.lines = [(1.0, "0, 1965, 2070, 800.1, 0x0, Not Active, Not Active, Not Active, Not Active"),
+               (2.0, "0, 1980, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active"),
+               (2.5, "garbage"),
+               (3.0, "0, 1200, 2070, 200.0, 0x1, Active, Not Active, Not Active, Not Active")]
+    c.t_start, c.t_stop = 0.5, 2.9    # the last sample came after the timed region
     s = c.summary()
     assert s["sm_mhz"] == 1972.5 and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
+    c.t_stop = None                   # no stop mark: every sample from the start on counts
+    s = c.summary()
+    assert s["samples"] == 3 and s["reasons"] == ["hw_slowdown", "sw_power_cap"]
 
 
 def _rank(rank, world, port, q):

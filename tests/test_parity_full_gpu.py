@@ -38,8 +38,35 @@ def _groups(wl, lens, n):
     return sorted(picks)
 
 
+# Kernel paths other than the default, each run once at full size on the
+# 32K grouped-query workload (split counts and ragged tails of a real launch).
+NON_DEFAULT_PATHS = {
+    "streamed": {"mma": 0, "full_staged": 0, "sparse_staged": 0},
+    "staged": {"mma": 0, "full_staged": 1, "sparse_staged": 1},
+    "prefetch2": {"mma": 1, "full_prefetch": 2},
+    "mma8": {"mma_full_tokens": 8},
+    "mma16": {"mma_sparse_tokens": 16},
+}
+
+
 @pytest.mark.parametrize("name,k,n_groups", CASES, ids=[f"{c[0]}-k{c[1]}" for c in CASES])
 def test_full_size_step_sampled(name, k, n_groups):
+    _step_against_oracle(name, k, n_groups)
+
+
+@pytest.mark.parametrize("path", list(NON_DEFAULT_PATHS))
+def test_full_size_step_on_non_default_kernel_paths(path):
+    try:
+        for key, value in NON_DEFAULT_PATHS[path].items():
+            td.td_set_tuning(key, value)
+        _step_against_oracle("llama3-8b-32k", None, 3)
+    finally:
+        for key in ("mma", "full_staged", "sparse_staged", "full_prefetch", "mma_full_tokens",
+                    "mma_sparse_tokens"):
+            td.td_set_tuning(key, -1)
+
+
+def _step_against_oracle(name, k, n_groups):
     wl = W.WORKLOADS[name]
     if k is not None:
         wl = wl.with_(top_k=k)

@@ -30,9 +30,11 @@ PATHS = {
     "streamed": {"full_staged": 0, "sparse_staged": 0, "mma": 0},
     "staged": {"full_staged": 1, "sparse_staged": 1, "mma": 0},
     "mma": {"mma": 1},
-    "prefetch2": {"mma": 1, "full_prefetch": 2},
+    "mma8": {"mma": 1, "mma_full_tokens": 8, "full_prefetch": 2},
+    "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},
 }
-TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch")
+TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch", "mma_full_tokens",
+               "mma_sparse_tokens")
 
 
 @pytest.fixture(scope="module", autouse=True, params=list(PATHS))
@@ -40,9 +42,11 @@ def staged(request):
     """Every case runs on each kernel path: CUDA-core kernels with
     register-streamed loads, the same with rows staged through shared memory,
     and the tensor-core kernels (grouped-query layers with G = 4, 8; other
-    groups keep the CUDA-core kernels); and the same with full layers
-    prefetching two rounds ahead into L2 (the default is one round on the
-    tensor cores, none on the CUDA cores)."""
+    groups keep the CUDA-core kernels) in three tilings: the default (16
+    tokens per warp per round for full and full+select layers, 8 for sparse
+    layers), 8 tokens per warp for every layer kind, and 16 for every layer
+    kind; the last two also prefetch two rounds ahead into L2 on full layers
+    (the default is one round)."""
     for key, value in PATHS[request.param].items():
         td.td_set_tuning(key, value)
     yield request.param
