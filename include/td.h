@@ -357,13 +357,22 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          (default 256)
  *   "topk_threads": 1024 (default) or 512 threads per top-k row (512: two
  *                   CTAs per SM); other values restore the default
+ *   "topk_cluster": CTAs per row of a top-k selection: 1 (one CTA
+ *          of "topk_threads"), or 2, 4, 8 (a thread-block cluster of
+ *          1024-thread CTAs, each scanning a slice of the row, merged through
+ *          distributed shared memory); other values restore the default
+ *          (for rows of at least 65536 positions, the largest cluster for
+ *          which rows x cluster fits one wave of SMs with at least 16384
+ *          positions per CTA; else 1)
  *   "pdl", "topk_pdl": 0 turns off programmatic dependent launch between a
  *                   call's kernels / before the top-k kernel (default 1)
  *   "mma_full_tokens", "mma_sparse_tokens": tokens each warp of a
  *          tensor-core full (and full+select) / sparse kernel takes per round:
  *          8 (CTAs of 8 warps) or 16 (CTAs of 4 warps, both row groups of the
- *          MMA); defaults 16 for full layers, 8 for sparse layers; other
- *          values restore the default
+ *          MMA); 32 takes 16 per round with two rounds in flight per warp
+ *          (the next round requested before this one's arithmetic); defaults
+ *          16 for full layers; for sparse layers 32 when a CTA gathers at
+ *          least 1024 rows, else 8; other values restore the default
  *   "wait_limit_us": microseconds after which a staged full-layer CTA stops
  *          waiting for a bulk copy (default 1 s).  A CTA that gives up waits
  *          (at the default limit) for every copy it issued, then joins the

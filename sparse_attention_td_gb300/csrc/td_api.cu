@@ -38,10 +38,13 @@ struct Tuning {
     int full_prefetch = -1;      // full / full+select layers: rounds ahead each warp prefetches into
                                  // L2 (register-streamed kernels); -1: 1 on the tensor cores, else 0
     int topk_warp_max = 0;       // top-k threshold bins up to this size finish in one warp (0: 256)
+    int topk_cluster = 0;        // CTAs per top-k row of a selection layer: 0 auto, 1, 2, 4, 8
     int pdl = 1;                 // 0: no programmatic dependent launch between a call's kernels
     int topk_pdl = 1;            // 0: the top-k kernel waits for its attention kernel in stream order
     int mma_full_tokens = 16;    // tensor-core full / full+select kernels: tokens per warp per round
-    int mma_sparse_tokens = 8;   // tensor-core sparse kernels: tokens per warp per round (8 or 16)
+    int mma_sparse_tokens = 0;   // tensor-core sparse kernels: tokens per warp per round (8, 16, or
+                                 // 32 = 16 with two rounds in flight); 0: 32 when a CTA's chunk
+                                 // holds >= kLongSparseChunk entries, else 8
     int wait_limit_us = 0;       // staged full layers: microseconds a stage wait may take before it
                                  // gives up and the launch reports TD_FLAG_WAIT_TIMEOUT (0: 1 s)
     int wait_test = 0;           // 1: each staged full-layer CTA's first wait polls a barrier that
@@ -67,9 +70,21 @@ int prefetch_for(int G)
     return g_tuning.full_prefetch < 0 ? (mma_for(G) ? 1 : 0) : g_tuning.full_prefetch;
 }
 
-int mma_tokens_for(bool sparse)
+// Measured on GB300: two rounds in flight per warp (16-token kernel, 2 CTAs
+// per SM) take 4% off sparse layers whose CTAs gather 2048 rows (serving
+// batch, k = 4096), are even at 1024 and lose 9-10% on CTAs of ~250 rows,
+// where the 8-token kernel (also 2 CTAs per SM, so the same split plan) stays.
+constexpr int kLongSparseChunk = 1024;
+
+// Tokens per warp per round of a tensor-core launch; chunk: index entries
+// per CTA of a sparse launch (its split plan is the same for 8 and 32).
+int mma_tokens_for(bool sparse, int chunk = 0)
 {
-    return sparse ? g_tuning.mma_sparse_tokens : g_tuning.mma_full_tokens;
+    if (!sparse)
+        return g_tuning.mma_full_tokens;
+    if (g_tuning.mma_sparse_tokens > 0)
+        return g_tuning.mma_sparse_tokens;
+    return chunk >= kLongSparseChunk ? 32 : 8;
 }
 
 bool staged_for(bool sparse, int G)
@@ -193,6 +208,30 @@ td_status check_shape(const td_shape *s)
 float effective_scale(const td_shape &s)
 {
     return s.scale != 0.0f ? s.scale : 1.0f / sqrtf((float)s.head_dim);
+}
+
+int device_sm_count();
+
+// CTAs per row of a top-k selection: a cluster of CS CTAs per row when rows
+// are long (at least kMinClusterRow positions), few enough for rows x CS CTAs
+// to fit one wave, and each CTA still scans at least kMinClusterSlice
+// positions; else one CTA per row.  Measured on GB300 (graph step): clusters
+// of 4 take 10 us off each 100K selection layer; at 10K and 32K they cost
+// 2-10 us a step, since the cluster's CTAs fill their SMs and the next
+// layer's CTAs cannot start early beside them.
+constexpr int kMinClusterRow = 65536;
+constexpr int kMinClusterSlice = 16384;
+int topk_cluster_for(const td_shape &s)
+{
+    if (g_tuning.topk_cluster > 0)
+        return g_tuning.topk_cluster;
+    const long rows = (long)s.batch * s.num_kv_heads;
+    if (s.max_seq_len < kMinClusterRow)
+        return 1;
+    for (int cs = 8; cs >= 2; cs /= 2)
+        if (rows * cs <= device_sm_count() && s.max_seq_len / cs >= kMinClusterSlice)
+            return cs;
+    return 1;
 }
 
 int device_sm_count()
@@ -365,7 +404,7 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
             t.row_k = ca.row_k;
             t.counts = cov.counts;
         }
-        if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads,
+        if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, topk_cluster_for(c.shape),
                             g_tuning.pdl != 0 && g_tuning.topk_pdl != 0, st) != cudaSuccess)
             return TD_ERR_CUDA;
     }
@@ -385,7 +424,7 @@ td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
     plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
     const cudaError_t le =
-        mma_for(c.G) ? td::launch_attention_mma(c.G, true, false, mma_tokens_for(true), a,
+        mma_for(c.G) ? td::launch_attention_mma(c.G, true, false, mma_tokens_for(true, a.chunk), a,
                                                 c.shape.batch, pdl, st)
                      : td::launch_attention(c.G, true, false, cluster, staged_for(true, c.G), a,
                                             c.shape.batch, pdl, st);
@@ -609,8 +648,8 @@ td_status td_topk_select(const td_shape *shape, const float *scores, const int32
     t.Nmax = c.shape.max_seq_len;
     t.top_k = top_k;
     t.warp_select_max = g_tuning.topk_warp_max;
-    if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, false, (cudaStream_t)stream) !=
-        cudaSuccess)
+    if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, topk_cluster_for(c.shape), false,
+                        (cudaStream_t)stream) != cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }
@@ -845,14 +884,19 @@ td_status td_set_tuning(const char *key, int32_t value)
     else if (!strcmp(key, "topk_pdl"))
         g_tuning.topk_pdl = value != 0 ? 1 : 0;
     else if (!strcmp(key, "mma_full_tokens"))
-        g_tuning.mma_full_tokens = (value == 8 || value == 16) ? value : kDefaultTuning.mma_full_tokens;
+        g_tuning.mma_full_tokens =
+            (value == 8 || value == 16 || value == 32) ? value : kDefaultTuning.mma_full_tokens;
     else if (!strcmp(key, "mma_sparse_tokens"))
         g_tuning.mma_sparse_tokens =
-            (value == 8 || value == 16) ? value : kDefaultTuning.mma_sparse_tokens;
+            (value == 8 || value == 16 || value == 32) ? value : kDefaultTuning.mma_sparse_tokens;
     else if (!strcmp(key, "wait_limit_us"))
         g_tuning.wait_limit_us = value > 0 ? value : kDefaultTuning.wait_limit_us;
     else if (!strcmp(key, "wait_test"))
         g_tuning.wait_test = value > 0 ? 1 : 0;
+    else if (!strcmp(key, "topk_cluster"))
+        g_tuning.topk_cluster = (value == 1 || value == 2 || value == 4 || value == 8)
+                                    ? value
+                                    : kDefaultTuning.topk_cluster;
     else if (!strcmp(key, "topk_threads"))
         g_tuning.topk_threads = (value == 512 || value == 1024) ? value : 0;
     else if (!strcmp(key, "attn_carveout"))

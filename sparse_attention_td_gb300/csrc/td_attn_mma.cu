@@ -327,15 +327,19 @@ attention_mma_kernel(const AttnArgs a)
 }
 
 // 16 tokens per warp per round, CTAs of 4 warps (kTokPerRound tokens a CTA
-// round), at most 168 registers for 3 CTAs per SM.  Fragment maps as in
-// attention_mma_kernel, with the MMAs' second row group filled: K of tokens
-// r and r + 8 (A rows r, r + 8 of S); V of tokens 2c, 2c+1, 2c+8, 2c+9 (the
-// P V k-step's 16 tokens); P of the same four tokens per head.
+// round).  Fragment maps as in attention_mma_kernel, with the MMAs' second
+// row group filled: K of tokens r and r + 8 (A rows r, r + 8 of S); V of
+// tokens 2c, 2c+1, 2c+8, 2c+9 (the P V k-step's 16 tokens); P of the same
+// four tokens per head.
+// DB = false: one round in flight per warp, at most 168 registers (3 CTAs per
+// SM).  DB = true: two register buffers, the next round's rows are requested
+// before this round's arithmetic (twice the bytes in flight per warp), at
+// most 255 registers (2 CTAs per SM).
 constexpr int kMma16Warps = kTokPerRound / 16;
 constexpr int kMma16Threads = kMma16Warps * 32;
 
-template <int G, bool SPARSE, bool SELECT>
-__global__ void __launch_bounds__(kMma16Threads, 3)
+template <int G, bool SPARSE, bool SELECT, bool DB>
+__global__ void __launch_bounds__(kMma16Threads, DB ? 2 : 3)
 attention_mma16_kernel(const AttnArgs a)
 {
     static_assert(G == 4 || G == 8, "heads of a group are the MMA's N = 8 columns");
@@ -417,9 +421,11 @@ attention_mma16_kernel(const AttnArgs a)
         prefetch_round_l2(kbase, vbase, base + warp * 16, lane, row_of);
         prefetch_round_l2(kbase, vbase, base + warp * 16 + 8, lane, row_of);
     };
-    uint2 kq0[2][8];
-    uint4 vv0[4][2];
+    uint2 kq0[2][8], kq1[2][8];
+    uint4 vv0[4][2], vv1[4][2];
     load(t0, kq0, vv0);  // the cache is never written by a kernel of the step
+    if constexpr (DB)
+        load(t0 + kTokPerRound, kq1, vv1);
     // full layers: rounds 1 .. prefetch go to L2 now, later rounds `prefetch`
     // ahead of use
     const int pf = SPARSE ? 0 : a.prefetch;
@@ -540,15 +546,30 @@ attention_mma16_kernel(const AttnArgs a)
         }
     };
 
-    if (t0 < t1)
-        round(t0, kq0, vv0);
-    for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
-        uint2 kq[2][8];
-        uint4 vv[4][2];
-        if (pf > 0)
-            prefetch(base + pf * kTokPerRound);
-        load(base, kq, vv);
-        round(base, kq, vv);
+    if constexpr (DB) {
+        // rounds in pairs: buffer 0 holds even rounds, buffer 1 odd ones; each
+        // buffer is refilled (two rounds ahead) right after its round's arithmetic
+        for (int base = t0; base < t1; base += 2 * kTokPerRound) {
+            if (pf > 0)
+                prefetch(base + pf * kTokPerRound);
+            round(base, kq0, vv0);
+            load(base + 2 * kTokPerRound, kq0, vv0);
+            if (base + kTokPerRound < t1) {
+                if (pf > 0)
+                    prefetch(base + (pf + 1) * kTokPerRound);
+                round(base + kTokPerRound, kq1, vv1);
+                load(base + 3 * kTokPerRound, kq1, vv1);
+            }
+        }
+    } else {
+        if (t0 < t1)
+            round(t0, kq0, vv0);
+        for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
+            if (pf > 0)
+                prefetch(base + pf * kTokPerRound);
+            load(base, kq0, vv0);
+            round(base, kq0, vv0);
+        }
     }
 
     pdl_launch_dependents();
@@ -621,21 +642,28 @@ int occupancy(Kern kern, int threads)
     return n > 0 ? n : 1;
 }
 
+// tokens: 8 (attention_mma_kernel), 16 (attention_mma16_kernel, one round in
+// flight per warp) or 32 (attention_mma16_kernel, two rounds in flight).
 template <int G, bool SPARSE, bool SELECT>
 cudaError_t launch_mma_one(int tokens, const AttnArgs &a, int batch, bool pdl, cudaStream_t st)
 {
-    return tokens == 16
-               ? launch_kernel(attention_mma16_kernel<G, SPARSE, SELECT>, kMma16Threads, a, batch,
-                               pdl, st)
-               : launch_kernel(attention_mma_kernel<G, SPARSE, SELECT>, kAttnThreads, a, batch,
-                               pdl, st);
+    if (tokens == 32)
+        return launch_kernel(attention_mma16_kernel<G, SPARSE, SELECT, true>, kMma16Threads, a,
+                             batch, pdl, st);
+    if (tokens == 16)
+        return launch_kernel(attention_mma16_kernel<G, SPARSE, SELECT, false>, kMma16Threads, a,
+                             batch, pdl, st);
+    return launch_kernel(attention_mma_kernel<G, SPARSE, SELECT>, kAttnThreads, a, batch, pdl, st);
 }
 
 template <int G, bool SPARSE, bool SELECT>
 int mma_occupancy_one(int tokens)
 {
-    return tokens == 16 ? occupancy(attention_mma16_kernel<G, SPARSE, SELECT>, kMma16Threads)
-                        : occupancy(attention_mma_kernel<G, SPARSE, SELECT>, kAttnThreads);
+    if (tokens == 32)
+        return occupancy(attention_mma16_kernel<G, SPARSE, SELECT, true>, kMma16Threads);
+    if (tokens == 16)
+        return occupancy(attention_mma16_kernel<G, SPARSE, SELECT, false>, kMma16Threads);
+    return occupancy(attention_mma_kernel<G, SPARSE, SELECT>, kAttnThreads);
 }
 
 template <int G>

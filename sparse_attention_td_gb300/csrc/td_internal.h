@@ -92,8 +92,10 @@ struct CoverageArgs {
 // kernel of the same call.
 cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, bool staged,
                              const AttnArgs &a, int batch, bool pdl, cudaStream_t stream);
-// threads: 1024 or 512 threads per row's CTA (0: 1024).
-cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, bool pdl,
+// threads: 1024 or 512 threads per row's CTA (0: 1024).  cluster: 2, 4 or 8
+// CTAs of 1024 threads per row, merged through distributed shared memory;
+// other values: one CTA per row.
+cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, int cluster, bool pdl,
                         cudaStream_t stream);
 cudaError_t launch_coverage(const CoverageArgs &a, int batch, bool pdl, cudaStream_t stream);
 
@@ -130,7 +132,8 @@ cudaError_t launch_probe_reads(const ProbeArgs &a, int batch, cudaStream_t strea
 // Tensor-core attention (mma.sync over a KV head's G query heads) for
 // G = 4 and 8: same arguments and results as launch_attention (no cluster
 // merge, register-fed fragments).  tokens: tokens a warp takes per round,
-// 8 (CTAs of 8 warps) or 16 (CTAs of 4 warps).
+// 8 (CTAs of 8 warps) or 16 (CTAs of 4 warps); 32: 16 per round with two
+// rounds in flight per warp.
 bool mma_supported(int G);
 cudaError_t launch_attention_mma(int G, bool sparse, bool select, int tokens, const AttnArgs &a,
                                  int batch, bool pdl, cudaStream_t stream);

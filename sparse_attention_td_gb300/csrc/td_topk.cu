@@ -26,6 +26,7 @@
 // aligned rows).  Rows longer than the bitmap, or a
 // threshold bin larger than the shared-memory buffer (heavily tied scores),
 // fall back to streaming passes and an ordered compaction of the row.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -74,6 +75,8 @@ struct TopkSmem {
     unsigned pre[kBatch * kWarps];
     unsigned res[2];                    // digit, remaining rank
     unsigned cand_count;
+    unsigned cut[2];                    // cluster path: the k-th key T and the largest kept position P
+    unsigned slice_total;               // cluster path: positions this CTA's slice keeps
     unsigned bitmap[kBitmapWords];      // selected positions of rows up to kTopkBitmapBits long
 };
 
@@ -287,36 +290,50 @@ __device__ uint32_t warp_select(unsigned *hist, unsigned n, ValF val, KeepF keep
     return prefix;
 }
 
+// Row length n of batch row b (clamped to [0, Nmax]; out-of-range lengths
+// are flagged once per batch row by `flag`).
+__device__ __forceinline__ int topk_row_len(const TopkArgs &a, int b, bool flag)
+{
+    int n = a.seq_lens[b];
+    if (n < 0 || n > a.Nmax) {
+        if (flag)
+            atomicOr(a.status, kFlagSeqLenOutOfRange);
+        n = n < 0 ? 0 : a.Nmax;
+    }
+    return n;
+}
+
+// Positions to select in row bg: top_k, or the row's budget (at most top_k).
+__device__ __forceinline__ int topk_row_budget(const TopkArgs &a, size_t bg)
+{
+    int k = a.top_k;
+    if (a.row_k) {
+        const int rk = __ldcg(a.row_k + bg);
+        k = rk < 0 ? 0 : (rk < a.top_k ? rk : a.top_k);
+    }
+    return k;
+}
+
+// The whole selection of row (b, KV head g) by one CTA of NT threads, with
+// the dynamic shared memory of topk_kernel<NT>.  Called after the wait for
+// the kernel that wrote the scores.
 template <int NT>
-__global__ void __launch_bounds__(NT, TopkCfg<NT>::kMinBlocks)
-topk_kernel(const TopkArgs a)
+__device__ void topk_row(const TopkArgs &a, int g, int b, unsigned char *smem_raw)
 {
     using C = TopkCfg<NT>;
     constexpr int kT = C::kT, kWarps = C::kWarps, kWordsPerThread = C::kWordsPerThread;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
     TopkSmem<NT> &sm = *reinterpret_cast<TopkSmem<NT> *>(smem_raw);
     uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem_raw + sizeof(TopkSmem<NT>));
     int32_t *cand_pos = reinterpret_cast<int32_t *>(cand_key + C::kCand);
 
-    const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const size_t bg = (size_t)b * a.Hkv + g;
     const int kcap = a.top_k;  // row length of the output
-    int n = a.seq_lens[b];
-    if (n < 0 || n > a.Nmax) {
-        if (tid == 0 && g == 0)
-            atomicOr(a.status, kFlagSeqLenOutOfRange);
-        n = n < 0 ? 0 : a.Nmax;
-    }
+    const int n = topk_row_len(a, b, tid == 0 && g == 0);
     const float *s = a.scores + bg * (size_t)a.Nmax;
     int32_t *out = a.idx + bg * (size_t)kcap;
-    pdl_wait();
-    pdl_launch_dependents();
-    int k = kcap;  // positions to select in this row (a per-row budget, at most kcap)
-    if (a.row_k) {
-        const int rk = __ldcg(a.row_k + bg);
-        k = rk < 0 ? 0 : (rk < kcap ? rk : kcap);
-    }
+    const int k = topk_row_budget(a, bg);  // positions to select in this row
     if (a.counts && tid == 0)
         a.counts[bg] = k < n ? k : n;
 
@@ -613,6 +630,301 @@ topk_kernel(const TopkArgs a)
     }
     for (int j = k + tid; j < kcap; j += kT)
         out[j] = -1;  // a per-row budget below the row length
+}
+
+// One CTA per row (grid: KV heads x batch rows).
+template <int NT>
+__global__ void __launch_bounds__(NT, TopkCfg<NT>::kMinBlocks)
+topk_kernel(const TopkArgs a)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    pdl_wait();
+    pdl_launch_dependents();
+    topk_row<NT>(a, blockIdx.x, blockIdx.y, smem_raw);
+}
+
+namespace cg = cooperative_groups;
+constexpr int kClusterNT = 1024;  // threads of each CTA of a row's cluster
+
+// A cluster of CS CTAs per row (grid: CS x KV heads x batch rows), for
+// launches with few, long rows, where one CTA per row would leave most SMs
+// idle.  Rank r takes the positions [r * L, (r + 1) * L) of the row (L a
+// multiple of 128): it marks the keys above the threshold bin in its slice of
+// the position bitmap (its own shared memory) and gathers the bin's (key,
+// position) pairs.  Rank 0 copies every rank's pairs through distributed
+// shared memory, finishes the select (T, P) as topk_row does, and every rank
+// reads the cut back, marks its selected pairs, and writes its slice of the
+// set after the counts of the slices before it.  The result is the same set,
+// in the same order, as topk_row.  Without the attention kernel's first-digit
+// histogram each rank counts its slice's and the ranks sum them.  A row whose
+// threshold bin exceeds the candidate buffer, a row longer than the bitmap,
+// or a row that keeps every position (or none), is done by rank 0 alone with
+// topk_row.
+template <int CS>
+__global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kClusterNT, 1)
+topk_cluster_kernel(const TopkArgs a)
+{
+    constexpr int NT = kClusterNT;
+    using C = TopkCfg<NT>;
+    constexpr int kT = C::kT;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    TopkSmem<NT> &sm = *reinterpret_cast<TopkSmem<NT> *>(smem_raw);
+    uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem_raw + sizeof(TopkSmem<NT>));
+    int32_t *cand_pos = reinterpret_cast<int32_t *>(cand_key + C::kCand);
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int g = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const size_t bg = (size_t)b * a.Hkv + g;
+
+    pdl_wait();
+    pdl_launch_dependents();
+    const int n = topk_row_len(a, b, rank == 0 && tid == 0 && g == 0);
+    const int k = topk_row_budget(a, bg);
+    if (n <= k || k == 0 || n > kTopkBitmapBits) {
+        if (rank == 0)
+            topk_row<NT>(a, g, b, smem_raw);
+        return;  // no rank touched another's shared memory
+    }
+    // this rank's slice of the row
+    const int L = ((n + CS - 1) / CS + 127) / 128 * 128;
+    const int lo = rank * L;
+    const int hi = min(n, lo + L);
+    const int len = hi > lo ? hi - lo : 0;
+    const float *s = a.scores + bg * (size_t)a.Nmax + lo;
+
+    unsigned *ghist = a.hist ? a.hist + bg * kBins1 : nullptr;
+    if (ghist) {
+        for (int i = tid; i < kBins1; i += kT)
+            sm.hist[i] = __ldcg(&ghist[i]);
+    } else {
+        // the slice's first-digit counts (sub-histograms in the candidate
+        // area), then the row's: every rank sums all ranks' counts
+        unsigned *sub = reinterpret_cast<unsigned *>(cand_key);
+        for (int i = tid; i < kSubHists * kBins1; i += kT)
+            sub[i] = 0u;
+        __syncthreads();
+        unsigned *mine = sub + (warp % kSubHists) * kBins1;
+        for (int base = 0; base < len; base += kT * kBatch) {
+            float v[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int i = base + j * kT + tid;
+                v[j] = i < len ? __ldcg(&s[i]) : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (base + j * kT + tid < len)
+                    atomicAdd(&mine[order_key(v[j]) >> (32 - kBits1)], 1u);
+        }
+        __syncthreads();
+        for (int i = tid; i < kBins1; i += kT) {
+            unsigned t = 0;
+            for (int h = 0; h < kSubHists; ++h)
+                t += sub[h * kBins1 + i];
+            sm.hist[i] = t;
+        }
+        cluster.sync();  // every rank's slice counts are in its sm.hist
+        unsigned *row_hist = sub;  // the sub-histograms are no longer needed
+        for (int i = tid; i < kBins1; i += kT) {
+            unsigned t = 0;
+            for (int rr = 0; rr < CS; ++rr)
+                t += *cluster.map_shared_rank(&sm.hist[i], rr);
+            row_hist[i] = t;
+        }
+        cluster.sync();  // nobody still reads another rank's slice counts
+        for (int i = tid; i < kBins1; i += kT)
+            sm.hist[i] = row_hist[i];
+    }
+    if (tid == 0)
+        sm.cand_count = 0u;
+    __syncthreads();
+    find_digit<kBins1>(sm, sm.hist, (unsigned)k);
+    const uint32_t d1 = sm.res[0];
+    const unsigned r1 = sm.res[1];
+    const unsigned bin_count = sm.hist[d1];
+    __syncthreads();
+    cluster.sync();  // every rank has read the histogram
+    if (bin_count > (unsigned)C::kCand) {
+        if (rank == 0)
+            topk_row<NT>(a, g, b, smem_raw);  // reads the histogram again and clears it
+        return;
+    }
+    if (rank == 0 && ghist)
+        for (int i = tid; i < kBins1; i += kT)
+            ghist[i] = 0u;  // leave the fused histogram zero for the next selection
+
+    for (int w = tid; w < (len + 31) / 32; w += kT)
+        sm.bitmap[w] = 0u;
+    __syncthreads();
+    const uint32_t prefix1 = d1 << (32 - kBits1);
+    const uint32_t mask1 = ~0u << (32 - kBits1);
+    const uint32_t top_of_bin = prefix1 | ~mask1;
+    // whole float4 groups (lo is a multiple of 128, so the slice keeps the
+    // row's 16-byte alignment): a warp covers 128 positions = 4 bitmap words
+    const int vec_n = (((uintptr_t)s & 15u) == 0) ? len / 4 : 0;
+    for (int base = 0; base < vec_n; base += kT * kBatchV) {
+        float4 v[kBatchV];
+#pragma unroll
+        for (int j = 0; j < kBatchV; ++j) {
+            const int i4 = base + j * kT + tid;
+            v[j] = i4 < vec_n ? __ldcg(reinterpret_cast<const float4 *>(s) + i4)
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int j = 0; j < kBatchV; ++j) {
+            const int i4 = base + j * kT + tid;
+            const int pos0 = 4 * i4;  // within the slice
+            const bool live = i4 < vec_n;
+            const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t key[4];
+            unsigned hitm = 0u, abovem = 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                key[e] = order_key(f[e]);
+                const uint32_t dg = key[e] >> (32 - kBits1);
+                hitm |= (live && dg == d1) ? (1u << e) : 0u;
+                abovem |= (live && dg > d1) ? (1u << e) : 0u;
+            }
+            unsigned word = abovem << (4 * (lane & 7));
+            word |= __shfl_xor_sync(kFull, word, 1);
+            word |= __shfl_xor_sync(kFull, word, 2);
+            word |= __shfl_xor_sync(kFull, word, 4);
+            if ((lane & 7) == 0 && live)
+                sm.bitmap[pos0 >> 5] = word;
+            if (hitm) {  // at most bin_count <= kCand hits in the row
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (hitm & (1u << e)) {
+                        const unsigned slot = atomicAdd(&sm.cand_count, 1u);
+                        cand_key[slot] = key[e];
+                        cand_pos[slot] = lo + pos0 + e;
+                    }
+            }
+        }
+    }
+    __syncthreads();  // whole-word stores above land before the tail ORs into a word
+    for (int i = 4 * vec_n + tid; i < len; i += kT) {  // the slice's last few scores
+        const uint32_t key = order_key(__ldcg(&s[i]));
+        if (key > top_of_bin)
+            atomicOr(&sm.bitmap[i >> 5], 1u << (i & 31));
+        else if ((key & mask1) == prefix1) {
+            const unsigned slot = atomicAdd(&sm.cand_count, 1u);
+            cand_key[slot] = key;
+            cand_pos[slot] = lo + i;
+        }
+    }
+    __syncthreads();
+    const unsigned own = sm.cand_count;
+    cluster.sync();  // every rank's pairs are complete
+
+    if (rank == 0) {
+        // gather the other ranks' pairs behind this rank's own, then select
+        unsigned total = own;
+        for (int rr = 1; rr < CS; ++rr) {
+            const unsigned cnt = *cluster.map_shared_rank(&sm.cand_count, rr);
+            const uint32_t *rk = cluster.map_shared_rank(cand_key, rr);
+            const int32_t *rp = cluster.map_shared_rank(cand_pos, rr);
+            for (unsigned i = tid; i < cnt; i += kT) {
+                cand_key[total + i] = rk[i];
+                cand_pos[total + i] = rp[i];
+            }
+            total += cnt;
+        }
+        __syncthreads();
+        uint32_t T;
+        int P = 0x7fffffff;
+        const unsigned warp_max =
+            a.warp_select_max > 0 ? (unsigned)a.warp_select_max : kWarpSelectMax;
+        if (total <= warp_max) {
+            if (warp == 0) {
+                unsigned need, neq;
+                T = warp_select(
+                    sm.hist, total, [&](unsigned i) { return cand_key[i]; },
+                    [&](unsigned) { return true; }, 31 - kBits1, prefix1, mask1, r1, &need, &neq);
+                if (need < neq) {
+                    unsigned r2, e2;
+                    P = (int)~warp_select(
+                        sm.hist, total, [&](unsigned i) { return ~(uint32_t)cand_pos[i]; },
+                        [&](unsigned i) { return cand_key[i] == T; }, 31, 0u, 0u, need, &r2, &e2);
+                }
+                if (lane == 0) {
+                    sm.cut[0] = T;
+                    sm.cut[1] = (unsigned)P;
+                }
+            }
+        } else {
+            auto cand_src = [&](auto f) {
+                for (unsigned i = tid; i < total; i += kT)
+                    f(cand_key[i], cand_pos[i]);
+            };
+            unsigned need_eq, n_eq;
+            T = radix_select(sm, cand_src, 31 - kBits1, prefix1, mask1, r1, &need_eq, &n_eq);
+            if (need_eq < n_eq) {
+                auto eq_src = [&](auto f) {
+                    for (unsigned i = tid; i < total; i += kT)
+                        if (cand_key[i] == T)
+                            f(~(uint32_t)cand_pos[i], 0);
+                };
+                unsigned r_dummy, e_dummy;
+                P = (int)~radix_select(sm, eq_src, 31, 0u, 0u, need_eq, &r_dummy, &e_dummy);
+            }
+            if (tid == 0) {
+                sm.cut[0] = T;
+                sm.cut[1] = (unsigned)P;
+            }
+        }
+    }
+    cluster.sync();  // the cut is in rank 0's shared memory; rank 0 is done reading the pairs
+    const uint32_t T = *cluster.map_shared_rank(&sm.cut[0], 0);
+    const int P = (int)*cluster.map_shared_rank(&sm.cut[1], 0);
+    for (unsigned i = tid; i < own; i += kT) {  // this rank's own pairs (the first `own`)
+        const uint32_t key = cand_key[i];
+        const int pos = cand_pos[i];
+        if (key > T || (key == T && pos <= P))
+            atomicOr(&sm.bitmap[(pos - lo) >> 5], 1u << ((pos - lo) & 31));
+    }
+    __syncthreads();
+    // positions kept by this slice, then their order within the slice
+    constexpr int kWordsPerThread = C::kWordsPerThread;
+    const int words = (len + 31) / 32;
+    unsigned w[kWordsPerThread];
+    unsigned count = 0;
+#pragma unroll
+    for (int j = 0; j < kWordsPerThread; ++j) {
+        const int wi = tid * kWordsPerThread + j;
+        w[j] = wi < words ? sm.bitmap[wi] : 0u;
+        count += __popc(w[j]);
+    }
+    unsigned slice_total;
+    unsigned slot = block_exclusive_sum(sm, count, &slice_total);
+    if (tid == 0)
+        sm.slice_total = slice_total;
+    cluster.sync();  // every slice's total is known
+    unsigned before = 0;
+    for (int rr = 0; rr < rank; ++rr)
+        before += *cluster.map_shared_rank(&sm.slice_total, rr);
+    cluster.sync();  // no rank leaves while another may still read its shared memory
+    const int kcap = a.top_k;
+    int32_t *out = a.idx + bg * (size_t)kcap;
+    slot += before;
+#pragma unroll
+    for (int j = 0; j < kWordsPerThread; ++j) {
+        unsigned word = w[j];
+        while (word) {
+            const int bit = __ffs(word) - 1;
+            word &= word - 1u;
+            if (slot < (unsigned)k)  // exactly k bits are set over all slices
+                out[slot] = lo + (tid * kWordsPerThread + j) * 32 + bit;
+            ++slot;
+        }
+    }
+    if (rank == 0) {
+        for (int j = k + tid; j < kcap; j += kT)
+            out[j] = -1;  // a per-row budget below the row length
+        if (a.counts && tid == 0)
+            a.counts[bg] = k;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1040,11 +1352,46 @@ cudaError_t launch_topk_nt(const TopkArgs &a, int batch, bool pdl, cudaStream_t 
     return cudaLaunchKernelEx(&cfg, topk_kernel<NT>, a);
 }
 
+template <int CS>
+cudaError_t launch_topk_cluster(const TopkArgs &a, int batch, bool pdl, cudaStream_t stream)
+{
+    constexpr size_t smem = topk_smem_bytes<kClusterNT>();
+    static bool configured[64] = {false};  // the smem opt-in is per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(topk_cluster_kernel<CS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < 64)
+            configured[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)CS, (unsigned)a.Hkv, (unsigned)batch);  // cluster dims: compiled in
+    cfg.blockDim = dim3(kClusterNT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<CS>, a);
+}
+
 }  // namespace
 
-cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, bool pdl,
+cudaError_t launch_topk(const TopkArgs &a, int batch, int threads, int cluster, bool pdl,
                         cudaStream_t stream)
 {
+    if (cluster == 2 || cluster == 4 || cluster == 8) {
+        return cluster == 8   ? launch_topk_cluster<8>(a, batch, pdl, stream)
+               : cluster == 4 ? launch_topk_cluster<4>(a, batch, pdl, stream)
+                              : launch_topk_cluster<2>(a, batch, pdl, stream);
+    }
     // Default 1024: with more rows than SMs, two 512-thread CTAs per SM take
     // every register of the SM, and the next layer's attention CTAs, launched
     // early by programmatic dependent launch, then find no room next to them;

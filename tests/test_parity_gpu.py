@@ -32,6 +32,7 @@ PATHS = {
     "mma": {"mma": 1},
     "mma8": {"mma": 1, "mma_full_tokens": 8, "full_prefetch": 2},
     "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},
+    "mma32": {"mma": 1, "mma_full_tokens": 32, "mma_sparse_tokens": 32},
 }
 TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch", "mma_full_tokens",
                "mma_sparse_tokens")
@@ -45,8 +46,9 @@ def staged(request):
     groups keep the CUDA-core kernels) in three tilings: the default (16
     tokens per warp per round for full and full+select layers, 8 for sparse
     layers), 8 tokens per warp for every layer kind, and 16 for every layer
-    kind; the last two also prefetch two rounds ahead into L2 on full layers
-    (the default is one round)."""
+    kind, these two also prefetching two rounds ahead into L2 on full layers
+    (the default is one round); and 16 tokens per warp with two rounds in
+    flight per warp for every layer kind."""
     for key, value in PATHS[request.param].items():
         td.td_set_tuning(key, value)
     yield request.param
@@ -59,17 +61,23 @@ def orc():
     return oracle.get()
 
 
-@pytest.fixture(params=[(1024, 0), (512, 0), (1024, 2048)], ids=["t1024", "t512", "t1024-warp2048"])
+@pytest.fixture(params=[(1024, 0, 1), (512, 0, 1), (1024, 2048, 1), (1024, 0, 2), (1024, 0, 4),
+                        (1024, 2048, 8)],
+                ids=["t1024", "t512", "t1024-warp2048", "cluster2", "cluster4", "cluster8-warp2048"])
 def topk_threads(request):
-    """Both block sizes of the top-k kernel, and the threshold-bin select taken
-    by one warp up to 2048 candidates instead of the default 256 (so the
-    adversarial rows run through both select paths)."""
-    threads, warp_max = request.param
+    """Both block sizes of the top-k kernel with one CTA per row, the
+    threshold-bin select taken by one warp up to 2048 candidates instead of
+    the default 256 (so the adversarial rows run through both select paths),
+    and clusters of 2, 4 and 8 CTAs per row (each scanning a slice of the
+    row, merged through distributed shared memory)."""
+    threads, warp_max, cluster = request.param
     td.td_set_tuning("topk_threads", threads)
     td.td_set_tuning("topk_warp_max", warp_max)
+    td.td_set_tuning("topk_cluster", cluster)
     yield threads
     td.td_set_tuning("topk_threads", 0)
     td.td_set_tuning("topk_warp_max", 0)
+    td.td_set_tuning("topk_cluster", 0)
 
 
 def _dev(*ts):
