@@ -330,6 +330,9 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
 /*
  * Kernel tuning knobs (process-wide, not thread-safe; for sweeps):
  *   "full_ctas_per_sm", "sparse_ctas_per_sm": resident CTAs assumed per SM
+ *          by the split plan (default: the occupancy of the kernel launched;
+ *          register-streamed sparse kernels that fit 4 or more per SM are
+ *          planned one below it, leaving room for the next layer's CTAs)
  *   "full_waves", "sparse_waves": target waves of CTAs per launch
  *   "max_splits": upper bound on splits per (batch, KV head)
  *   "cluster": 1 merges a (batch, KV head)'s splits (when 2..8) through a
@@ -342,8 +345,15 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *                  registers; negative restores the default (staged when
  *                  num_q_heads / num_kv_heads >= 4)
  *   "sparse_staged": 1 stages the gathered rows of sparse layers through a
- *                  per-thread cp.async ring in shared memory; 0 (default) or
- *                  negative streams them into registers
+ *                  per-thread cp.async ring in shared memory; 2 through TMA
+ *                  row gathers (cp.async.bulk.tensor tile::gather4, four
+ *                  rows per copy) into the same ring (a launch whose cache
+ *                  rows B x Hkv x Nmax reach 2^31, or a cache not 16-byte
+ *                  aligned, returns TD_ERR_UNSUPPORTED_SHAPE); 0 streams them
+ *                  into registers; negative (default) takes 1 when every CTA
+ *                  of the register-streamed plan would gather at most 64
+ *                  rows, else 0.  Applies to the CUDA-core kernels (not to
+ *                  G = 4, 8 on the tensor cores)
  *   "mma": 1 (and the default) runs grouped-query layers with G = 4 or 8 on
  *          the tensor cores (mma.sync over the group's heads); 0 on the CUDA
  *          cores (where "full_staged" / "sparse_staged" apply); negative

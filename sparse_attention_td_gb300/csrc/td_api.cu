@@ -7,6 +7,7 @@
 // overwrites the resident index buffer), and PPSA layers run the sparse
 // attention kernel over the most recent selection (§三 "Position Persistent
 // Sparse Attention": later layers reuse the selected positions).
+#include <cuda.h>  // tensor-map types only: the encoder is reached through the runtime
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -32,8 +33,10 @@ struct Tuning {
     int topk_threads = 0;        // 0 = 1024 threads per row, or 512
     int full_staged = -1;        // 1: full / full+select kernels stage K/V through shared memory
                                  // (bulk copies); 0: register-streamed; -1: staged when G >= 4
-    int sparse_staged = 0;       // 1: sparse kernels stage the gathered rows through shared memory
-                                 // (per-thread cp.async ring); 0: register-streamed
+    int sparse_staged = -1;      // CUDA-core sparse kernels: 1 stage the gathered rows through
+                                 // shared memory (per-thread cp.async ring); 2 through TMA row
+                                 // gathers (tile::gather4); 0 register-streamed; -1 auto (1 for
+                                 // small layers, see staged_for)
     int mma = -1;                // 1 / -1 (default): tensor-core kernels for G = 4, 8; 0: CUDA cores
     int full_prefetch = -1;      // full / full+select layers: rounds ahead each warp prefetches into
                                  // L2 (register-streamed kernels); -1: 1 on the tensor cores, else 0
@@ -87,17 +90,71 @@ int mma_tokens_for(bool sparse, int chunk = 0)
     return chunk >= kLongSparseChunk ? 32 : 8;
 }
 
-bool staged_for(bool sparse, int G)
+int device_sm_count();
+
+// How a CUDA-core launch gets its K/V rows (0 registers, 1 staged, 2 TMA
+// row gathers for sparse layers).  Measured on GB300 (graph step), sparse
+// layers: staging through a per-thread cp.async ring takes the 10K MHA step
+// from 316 to 289 us, where every CTA of the register plan would gather one
+// round (64 rows) or less; on longer CTAs (100K: ~3.5 rounds) it costs 2%.
+int staged_for(const td_shape &s, bool sparse, long n_total)
 {
-    if (sparse)
-        return g_tuning.sparse_staged > 0;
-    return g_tuning.full_staged < 0 ? G >= 4 : g_tuning.full_staged > 0;
+    const int G = s.num_q_heads / s.num_kv_heads;
+    if (!sparse)
+        return (g_tuning.full_staged < 0 ? G >= 4 : g_tuning.full_staged > 0) ? 1 : 0;
+    if (g_tuning.sparse_staged >= 0)
+        return g_tuning.sparse_staged;
+    const long units = (long)s.batch * s.num_kv_heads;
+    const long slots = (long)device_sm_count() * td::attention_ctas_per_sm(G, true, false, 0);
+    return units * n_total <= slots * td::kTokPerRound ? 1 : 0;
 }
+
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline long ceil_div(long a, long b) { return (a + b - 1) / b; }
+
+// cuTensorMapEncodeTiled, reached through the runtime (the library does not
+// link the driver library itself); null if the driver does not provide it.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return (EncodeTiledFn)p;
+    }();
+    return fn;
+}
+
+// Tensor map over a cache's rows for TMA row gathers: a 2D bf16 tensor of
+// `rows` rows of 128 values (256-byte stride), box 128 x 1 (one row: the
+// only box height a tile::gather4 copy takes), no swizzle (a half-warp reads
+// a whole 256-byte row, so the stage layout has no bank conflicts), zero fill
+// for rows past the end.
+bool encode_row_map(td::TmaDesc *out, const void *base, long rows)
+{
+    static_assert(sizeof(td::TmaDesc) == sizeof(CUtensorMap), "opaque tensor-map size");
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn || rows < 1 || rows >= (1L << 31) || !aligned(base, 16))
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, 1};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(reinterpret_cast<CUtensorMap *>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+              const_cast<void *>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // Largest split count a launch of `n_total` tokens/entries may use.
 int split_cap(long units, long n_total, bool sparse)
@@ -257,9 +314,17 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
     const int G = s.num_q_heads / s.num_kv_heads;
     const long units = (long)s.batch * s.num_kv_heads;
     int per_sm = sparse ? g_tuning.sparse_ctas_per_sm : g_tuning.full_ctas_per_sm;
-    if (per_sm <= 0)
+    if (per_sm <= 0) {
+        const int staged = mma_for(G) ? 0 : staged_for(s, sparse, n_total);
         per_sm = mma_for(G) ? td::attention_mma_ctas_per_sm(G, sparse, select, mma_tokens_for(sparse))
-                            : td::attention_ctas_per_sm(G, sparse, select, staged_for(sparse, G));
+                            : td::attention_ctas_per_sm(G, sparse, select, staged);
+        // Measured on GB300 (graph step): register-streamed sparse layers
+        // planned one CTA per SM below the 4+ that fit leave a slot for the
+        // next layer's CTAs to start early (100K MHA step 1438 -> 1426 us);
+        // at 2 per SM the launch loses half its warps and is slower.
+        if (sparse && !mma_for(G) && staged == 0 && per_sm >= 4)
+            per_sm -= 1;
+    }
     const long slots = (long)device_sm_count() * per_sm;  // resident CTAs per wave
     int waves = sparse ? g_tuning.sparse_waves : g_tuning.full_waves;
     if (waves <= 0)  // one wave of long CTAs when the pairs are few; more, shorter
@@ -372,7 +437,8 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
     const cudaError_t le =
         mma_for(c.G) ? td::launch_attention_mma(c.G, false, select, mma_tokens_for(false), a,
                                                 c.shape.batch, pdl, st)
-                     : td::launch_attention(c.G, false, select, cluster, staged_for(false, c.G), a,
+                     : td::launch_attention(c.G, false, select, cluster,
+                                            staged_for(c.shape, false, c.shape.max_seq_len), a,
                                             c.shape.batch, pdl, st);
     if (le != cudaSuccess)
         return TD_ERR_CUDA;
@@ -423,10 +489,17 @@ td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
     a.idx_dep = idx_dep ? 1 : 0;
     plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
+    const int staged = staged_for(c.shape, true, top_k);
+    if (!mma_for(c.G) && !cluster && staged == 2) {
+        const long rows = (long)c.shape.batch * c.shape.num_kv_heads * c.shape.max_seq_len;
+        if (!encode_row_map(&a.tma_k, k, rows) || !encode_row_map(&a.tma_v, v, rows))
+            return TD_ERR_UNSUPPORTED_SHAPE;
+        a.tma_rows = (int)rows;
+    }
     const cudaError_t le =
         mma_for(c.G) ? td::launch_attention_mma(c.G, true, false, mma_tokens_for(true, a.chunk), a,
                                                 c.shape.batch, pdl, st)
-                     : td::launch_attention(c.G, true, false, cluster, staged_for(true, c.G), a,
+                     : td::launch_attention(c.G, true, false, cluster, staged, a,
                                             c.shape.batch, pdl, st);
     if (le != cudaSuccess)
         return TD_ERR_CUDA;
@@ -872,7 +945,7 @@ td_status td_set_tuning(const char *key, int32_t value)
     else if (!strcmp(key, "full_staged"))
         g_tuning.full_staged = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.full_staged);  // <0: auto
     else if (!strcmp(key, "sparse_staged"))
-        g_tuning.sparse_staged = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.sparse_staged);
+        g_tuning.sparse_staged = (value >= 0 && value <= 2) ? value : kDefaultTuning.sparse_staged;
     else if (!strcmp(key, "mma"))
         g_tuning.mma = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.mma);
     else if (!strcmp(key, "full_prefetch"))

@@ -19,11 +19,14 @@
 // shuffles.  The rows reach the registers one of two ways:
 //   * register-streamed: 16-byte loads straight from HBM, 4 tokens of K and V
 //     in flight per thread (32 KB per CTA);
-//   * staged: bulk asynchronous copies (the TMA engine's cp.async.bulk, one
-//     256-byte copy per gathered row, one copy per K or V block of contiguous
-//     rows) fill a ring of shared-memory stages of 64 tokens, completing on
-//     an mbarrier; the CTA computes on stage i while stages i+1.. are in
-//     flight (up to 128 KB per CTA).
+//   * staged: asynchronous copies fill a ring of shared-memory stages of 64
+//     tokens, completing on an mbarrier; the CTA computes on stage i while
+//     stages i+1.. are in flight (up to 128 KB per CTA).  Full layers: one
+//     bulk copy (cp.async.bulk) per K or V block of contiguous rows.  Sparse
+//     layers: either per-thread cp.async of the 16-byte pieces each thread
+//     reads (STAGED = 1), or TMA row gathers (cp.async.bulk.tensor
+//     tile::gather4: four cache rows per copy, through a tensor map over the
+//     cache's rows; STAGED = 2).
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -98,6 +101,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
     }
 }
 
+// Four rows of a 2D tensor map (rows of 128 bf16 values, box 128 x 1) into
+// 1024 contiguous bytes of shared memory, counted on `bar` in bytes.  The
+// column coordinate is 0; a row coordinate past the map's last row reads
+// zeros (and still counts its 256 bytes).
+__device__ __forceinline__ void tma_gather4(void *dst, const TmaDesc *map, int r0, int r1, int r2,
+                                            int r3, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Global -> shared bulk copy (16-byte aligned addresses, size a multiple of
 // 16) whose completion is counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, unsigned bytes,
@@ -139,13 +156,16 @@ namespace cg = cooperative_groups;
 // CLUSTER: the splits of one (batch row, KV head) form a thread-block
 // cluster (grid x = cluster x = splits) and are merged through distributed
 // shared memory; otherwise through global partials and an arrival ticket.
-// STAGED: rows reach shared memory by bulk copies (see the file comment).
-template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
+// STAGED: 0 register-streamed; 1 rows reach shared memory by bulk copies
+// (full layers) or per-thread cp.async (sparse layers); 2 (sparse layers
+// only) by TMA row gathers (see the file comment).
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER, int STAGED>
 // Register budgets: 64 (MHA, 4 CTAs per SM; 85 and 3 CTAs with selection), 128 (G = 2, 4:
 // 2 CTAs per SM), 255 (G = 8).
 __global__ void __launch_bounds__(kAttnThreads, G == 1 ? (SELECT ? 3 : 4) : (G <= 4 ? 2 : 1))
-attention_kernel(const AttnArgs a)
+attention_kernel(const __grid_constant__ AttnArgs a)
 {
+    static_assert(STAGED != 2 || SPARSE, "TMA row gathers serve sparse layers");
     constexpr int U = kTokPerHalf;
     constexpr int S = staged_stages(G);
     extern __shared__ __align__(128) unsigned char sm_stage[];  // STAGED: [S][K rows | V rows]
@@ -237,19 +257,40 @@ attention_kernel(const AttnArgs a)
     const int n_it = t1 > t0 ? (t1 - t0 + kTokPerRound - 1) / kTokPerRound : 0;
     const uint16_t *krows = a.k + bg * (size_t)a.Nmax * kHeadDim;
     const uint16_t *vrows = a.v + bg * (size_t)a.Nmax * kHeadDim;
-    auto issue_stage = [&](int it) {  // full layers, warp 0
+    auto issue_stage = [&](int it) {  // warp 0
         unsigned char *kst = sm_stage + (it % S) * kStageBytes;
         unsigned char *vst = kst + kStageBytes / 2;
         uint64_t *bar = &sm_full[it % S];
         const int base = t0 + it * kTokPerRound;
-        // contiguous rows: one copy for the K block, one for the V block
-        const int n = min(kTokPerRound, t1 - base);
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar, (unsigned)n * kStageTxPerToken);
-            bulk_copy_g2s(kst, krows + (size_t)base * kHeadDim, (unsigned)n * kStageRowBytes,
-                          bar);
-            bulk_copy_g2s(vst, vrows + (size_t)base * kHeadDim, (unsigned)n * kStageRowBytes,
-                          bar);
+        if constexpr (SPARSE) {
+            // STAGED == 2: the stage's 64 rows of K and of V, four per gather,
+            // one gather per lane of warp 0 (lanes 0-15 K, 16-31 V); padding
+            // and tokens past the split read the zero rows past the map.
+            // Lane 0 announces the stage's bytes before any gather is issued.
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar, (unsigned)kTokPerRound * kStageTxPerToken);
+            __syncwarp();
+            const int oob = a.tma_rows;  // first row past the map
+            const int row0 = (int)(bg * (size_t)a.Nmax);
+            auto grow = [&](int t) {
+                const int p = t < t1 ? sm_rows[t - t0] : -1;
+                return p >= 0 ? row0 + p : oob;
+            };
+            const int j = lane & 15;
+            const int t = base + 4 * j;
+            tma_gather4((lane < 16 ? kst : vst) + j * 4 * kStageRowBytes,
+                        lane < 16 ? &a.tma_k : &a.tma_v, grow(t), grow(t + 1), grow(t + 2),
+                        grow(t + 3), bar);
+        } else {
+            // contiguous rows: one copy for the K block, one for the V block
+            const int n = min(kTokPerRound, t1 - base);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar, (unsigned)n * kStageTxPerToken);
+                bulk_copy_g2s(kst, krows + (size_t)base * kHeadDim, (unsigned)n * kStageRowBytes,
+                              bar);
+                bulk_copy_g2s(vst, vrows + (size_t)base * kHeadDim, (unsigned)n * kStageRowBytes,
+                              bar);
+            }
         }
     };
 
@@ -284,7 +325,7 @@ attention_kernel(const AttnArgs a)
     // requested before waiting for the previous kernel; q may come from it.
     uint4 kr0[U], vr0[U];
     bool ok0[U];
-    if constexpr (STAGED && SPARSE) {
+    if constexpr (STAGED == 1 && SPARSE) {
         for (int it = 0; it < S; ++it)
             issue_rows_cp(it);
     } else if constexpr (STAGED) {
@@ -437,7 +478,7 @@ attention_kernel(const AttnArgs a)
             }
         }
     };
-    if constexpr (STAGED && SPARSE) {
+    if constexpr (STAGED == 1 && SPARSE) {
         const int slot0 = (warp * 2 + half) * U;
         for (int it = 0; it < n_it; ++it) {
             cp_async_wait<S - 1>();  // this thread's copies of stage `it` have landed
@@ -649,14 +690,14 @@ attention_kernel(const AttnArgs a)
 
 int g_carveout = -1;  // preferred shared-memory carveout (percent) for the attention kernels
 
-template <int G, bool STAGED>
+template <int G, int STAGED>
 constexpr size_t dyn_smem_bytes()
 {
     return STAGED ? (size_t)staged_stages(G) * kStageBytes : 0;
 }
 
 // The dynamic shared-memory opt-in of the staged kernels, once per device.
-template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER, int STAGED>
 cudaError_t configure_once()
 {
     if (!STAGED)
@@ -676,7 +717,7 @@ cudaError_t configure_once()
     return e;
 }
 
-template <int G, bool SPARSE, bool SELECT, bool CLUSTER, bool STAGED>
+template <int G, bool SPARSE, bool SELECT, bool CLUSTER, int STAGED>
 cudaError_t launch_one(const AttnArgs &a, int batch, bool pdl, cudaStream_t stream)
 {
     auto kern = attention_kernel<G, SPARSE, SELECT, CLUSTER, STAGED>;
@@ -711,7 +752,7 @@ cudaError_t launch_one(const AttnArgs &a, int batch, bool pdl, cudaStream_t stre
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int G, bool SPARSE, bool SELECT, bool STAGED>
+template <int G, bool SPARSE, bool SELECT, int STAGED>
 int occupancy_one()
 {
     int n = 0;
@@ -726,17 +767,20 @@ int occupancy_one()
 
 // The cluster merge is built for the register-streamed kernels.
 template <int G, bool SPARSE, bool SELECT>
-cudaError_t launch_mode(bool cluster, bool staged, const AttnArgs &a, int batch, bool pdl,
+cudaError_t launch_mode(bool cluster, int staged, const AttnArgs &a, int batch, bool pdl,
                         cudaStream_t st)
 {
     if (cluster)
-        return launch_one<G, SPARSE, SELECT, true, false>(a, batch, pdl, st);
-    return staged ? launch_one<G, SPARSE, SELECT, false, true>(a, batch, pdl, st)
-                  : launch_one<G, SPARSE, SELECT, false, false>(a, batch, pdl, st);
+        return launch_one<G, SPARSE, SELECT, true, 0>(a, batch, pdl, st);
+    if constexpr (SPARSE)
+        if (staged == 2)
+            return launch_one<G, SPARSE, SELECT, false, 2>(a, batch, pdl, st);
+    return staged ? launch_one<G, SPARSE, SELECT, false, 1>(a, batch, pdl, st)
+                  : launch_one<G, SPARSE, SELECT, false, 0>(a, batch, pdl, st);
 }
 
 template <int G>
-cudaError_t launch_g(bool sparse, bool select, bool cluster, bool staged, const AttnArgs &a,
+cudaError_t launch_g(bool sparse, bool select, bool cluster, int staged, const AttnArgs &a,
                      int batch, bool pdl, cudaStream_t st)
 {
     if (sparse)
@@ -750,7 +794,7 @@ cudaError_t launch_g(bool sparse, bool select, bool cluster, bool staged, const 
 
 void set_attention_carveout(int percent) { g_carveout = percent; }
 
-cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, bool staged,
+cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, int staged,
                              const AttnArgs &a, int batch, bool pdl, cudaStream_t stream)
 {
     switch (G) {
@@ -767,18 +811,19 @@ cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, bool
     }
 }
 
-int attention_ctas_per_sm(int G, bool sparse, bool select, bool staged)
+int attention_ctas_per_sm(int G, bool sparse, bool select, int staged)
 {
 #define TD_OCC_G(GG)                                                                      \
     case GG:                                                                              \
         if (sparse)                                                                       \
-            return staged ? occupancy_one<GG, true, false, true>()                        \
-                          : occupancy_one<GG, true, false, false>();                      \
+            return staged == 2 ? occupancy_one<GG, true, false, 2>()                      \
+                               : (staged ? occupancy_one<GG, true, false, 1>()            \
+                                         : occupancy_one<GG, true, false, 0>());          \
         if (select)                                                                       \
-            return staged ? occupancy_one<GG, false, true, true>()                        \
-                          : occupancy_one<GG, false, true, false>();                      \
-        return staged ? occupancy_one<GG, false, false, true>()                           \
-                      : occupancy_one<GG, false, false, false>();
+            return staged ? occupancy_one<GG, false, true, 1>()                           \
+                          : occupancy_one<GG, false, true, 0>();                          \
+        return staged ? occupancy_one<GG, false, false, 1>()                              \
+                      : occupancy_one<GG, false, false, 0>();
     switch (G) {
         TD_OCC_G(1)
         TD_OCC_G(2)

@@ -29,6 +29,11 @@ constexpr uint32_t kFlagIndexOutOfRange = 0x1u;
 constexpr uint32_t kFlagSeqLenOutOfRange = 0x2u;
 constexpr uint32_t kFlagWaitTimeout = 0x4u;  // a bounded wait for an async copy gave up
 
+// A TMA tensor map (the driver's CUtensorMap: 128 opaque bytes, 64-byte aligned).
+struct alignas(64) TmaDesc {
+    unsigned char bytes[128];
+};
+
 // One attention launch (full or sparse).  Partials are struct-of-arrays over
 // (batch*kv_head, split, head-in-group[, dim]) with split stride `nsplit`.
 struct AttnArgs {
@@ -55,6 +60,8 @@ struct AttnArgs {
     int wait_test;           // staged full layers: each CTA's first wait polls a barrier nothing
                              // arrives on (tests of the failure report); 0 in normal use
     float scale;             // softmax scale (natural-log units)
+    int tma_rows;            // sparse, row gathers: rows of the maps (B * Hkv * Nmax)
+    TmaDesc tma_k, tma_v;    // sparse, row gathers: maps over the K / V cache rows
 };
 
 struct TopkArgs {
@@ -85,12 +92,13 @@ struct CoverageArgs {
 // G = query heads per KV head (1, 2, 4, 8).
 // cluster: merge the splits through a thread-block cluster (requires
 // a.nsplit <= kMaxClusterSplits); otherwise through global partials.
-// staged: K/V rows reach shared memory by bulk asynchronous copies into a
-// ring of stages (ignored when cluster is set); otherwise register-streamed.
+// staged: K/V rows reach shared memory through a ring of stages (ignored when
+// cluster is set): 1 by bulk copies (full) or per-thread cp.async (sparse),
+// 2 (sparse) by TMA row gathers through a.tma_k / a.tma_v; 0 register-streamed.
 // pdl: the launch may overlap the tail of the kernel before it on the stream
 // (programmatic dependent launch); only for a kernel whose predecessor is a
 // kernel of the same call.
-cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, bool staged,
+cudaError_t launch_attention(int G, bool sparse, bool select, bool cluster, int staged,
                              const AttnArgs &a, int batch, bool pdl, cudaStream_t stream);
 // threads: 1024 or 512 threads per row's CTA (0: 1024).  cluster: 2, 4 or 8
 // CTAs of 1024 threads per row, merged through distributed shared memory;
@@ -143,6 +151,6 @@ int attention_mma_ctas_per_sm(int G, bool sparse, bool select, int tokens);
 void set_attention_carveout(int percent);
 
 // Resident CTAs per SM of one attention instantiation (occupancy query).
-int attention_ctas_per_sm(int G, bool sparse, bool select, bool staged);
+int attention_ctas_per_sm(int G, bool sparse, bool select, int staged);
 
 }  // namespace td

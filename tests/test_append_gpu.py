@@ -32,6 +32,7 @@ def orc():
 PATHS = {
     "streamed": {"full_staged": 0, "sparse_staged": 0, "mma": 0},
     "staged": {"full_staged": 1, "sparse_staged": 1, "mma": 0},
+    "tma": {"full_staged": 1, "sparse_staged": 2, "mma": 0},
     "mma": {"mma": 1},
     "mma8": {"mma": 1, "mma_full_tokens": 8, "full_prefetch": 2},
     "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},

@@ -43,10 +43,12 @@ def _groups(wl, lens, n):
 NON_DEFAULT_PATHS = {
     "streamed": {"mma": 0, "full_staged": 0, "sparse_staged": 0},
     "staged": {"mma": 0, "full_staged": 1, "sparse_staged": 1},
+    "tma": {"mma": 0, "sparse_staged": 2},
     "prefetch2": {"mma": 1, "full_prefetch": 2},
     "mma8": {"mma_full_tokens": 8},
     "mma16": {"mma_sparse_tokens": 16},
 }
+PATH_CASES = [(p, "llama3-8b-32k") for p in NON_DEFAULT_PATHS] + [("tma", "llama2-7b-100k")]
 
 
 @pytest.mark.parametrize("name,k,n_groups", CASES, ids=[f"{c[0]}-k{c[1]}" for c in CASES])
@@ -54,12 +56,12 @@ def test_full_size_step_sampled(name, k, n_groups):
     _step_against_oracle(name, k, n_groups)
 
 
-@pytest.mark.parametrize("path", list(NON_DEFAULT_PATHS))
-def test_full_size_step_on_non_default_kernel_paths(path):
+@pytest.mark.parametrize("path,workload", PATH_CASES, ids=[f"{p}-{w}" for p, w in PATH_CASES])
+def test_full_size_step_on_non_default_kernel_paths(path, workload):
     try:
         for key, value in NON_DEFAULT_PATHS[path].items():
             td.td_set_tuning(key, value)
-        _step_against_oracle("llama3-8b-32k", None, 3)
+        _step_against_oracle(workload, None, 3)
     finally:
         for key in ("mma", "full_staged", "sparse_staged", "full_prefetch", "mma_full_tokens",
                     "mma_sparse_tokens"):

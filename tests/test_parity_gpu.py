@@ -29,6 +29,7 @@ def _built():
 PATHS = {
     "streamed": {"full_staged": 0, "sparse_staged": 0, "mma": 0},
     "staged": {"full_staged": 1, "sparse_staged": 1, "mma": 0},
+    "tma": {"full_staged": 1, "sparse_staged": 2, "mma": 0},
     "mma": {"mma": 1},
     "mma8": {"mma": 1, "mma_full_tokens": 8, "full_prefetch": 2},
     "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},
@@ -41,8 +42,9 @@ TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch", "mma_full
 @pytest.fixture(scope="module", autouse=True, params=list(PATHS))
 def staged(request):
     """Every case runs on each kernel path: CUDA-core kernels with
-    register-streamed loads, the same with rows staged through shared memory,
-    and the tensor-core kernels (grouped-query layers with G = 4, 8; other
+    register-streamed loads, the same with rows staged through shared memory
+    (bulk copies for full layers; per-thread cp.async, or TMA row gathers, for
+    sparse layers), and the tensor-core kernels (grouped-query layers with G = 4, 8; other
     groups keep the CUDA-core kernels) in three tilings: the default (16
     tokens per warp per round for full and full+select layers, 8 for sparse
     layers), 8 tokens per warp for every layer kind, and 16 for every layer
