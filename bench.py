@@ -281,8 +281,9 @@ def attn_source_hash() -> str:
 
 def measured_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of one attention kernel ("full" or "sparse") from
-    a committed ncu summary, or None if there is none for this workload or the
-    kernel source changed since it was taken."""
+    a committed ncu summary, or None if there is none for this workload (name,
+    or name-k<top_k> for another k than the workload's own) or the kernel
+    source changed since it was taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -551,30 +552,29 @@ def run_ours(args, world, rank, local):
     step_sum = sum(by_mode[k] * counts[k] for k in by_mode)
     kernels = {}
     full_launch_us = by_mode.get("full", by_mode.get("full_select"))
-    tensor = wl.group in (4, 8)  # grouped-query layers run on the tensor-core kernels
     kernels["full"] = {
-        "kernel": ("attention_mma16_kernel<G,full> (tensor cores, 16 tokens per warp; "
-                   if tensor else "attention_kernel<G,full> (CUDA cores; ")
-                  + "split-K flash decode over all N_b tokens + combine)",
+        "kernel": td.td_kernel_name(shape, 0, False)
+                  + ": split-K flash decode over all N_b tokens + combine",
         "launch_us": full_launch_us, "bytes": bytes_model["per_launch"]["full"],
         "floor_us": floor_by_mode.get("full", floor_by_mode.get("full_select")),
         "share": (full_launch_us * (counts["full"] + counts["full_select"])) / step_sum}
     if "sparse" in by_mode:
         kernels["sparse"] = {
-            "kernel": ("attention_mma_kernel<G,sparse> (tensor cores, 8 tokens per warp; "
-                       if tensor else "attention_kernel<G,sparse> (CUDA cores; ")
-                      + "gather of the k persisted K/V rows + combine)",
+            "kernel": td.td_kernel_name(shape, wl.top_k, True)
+                      + ": gather of the k persisted K/V rows + combine",
             "launch_us": by_mode["sparse"], "bytes": bytes_model["per_launch"]["sparse"],
             "floor_us": floor_by_mode["sparse"],
             "share": by_mode["sparse"] * counts["sparse"] / step_sum}
     rooflines = {}
+    # ncu summaries are keyed by workload, and by k where it is not the workload's own
+    traffic_key = wl.name if wl.top_k == W.WORKLOADS[wl.name].top_k else f"{wl.name}-k{wl.top_k}"
     for name, kk in kernels.items():
         ach = kk["bytes"] / (kk["launch_us"] * 1e-6) / 1e9
         rooflines[name] = {
             "kernel": kk["kernel"], "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
             "unit": "GB/s", "frac": round(ach / peak, 4),
             "frac_of_nominal": round(ach / NOMINAL_HBM_GBS, 4),
-            "traffic": measured_traffic(wl.name, name), "peak_source": f"{peak_kind} hbm_gbs",
+            "traffic": measured_traffic(traffic_key, name), "peak_source": f"{peak_kind} hbm_gbs",
             "algorithmic_bytes_per_launch": kk["bytes"], "launch_us": round(kk["launch_us"], 2),
             "read_floor_us": round(kk["floor_us"], 2),
             "frac_of_read_floor": round(kk["floor_us"] / kk["launch_us"], 4),

@@ -402,6 +402,13 @@ td_status td_set_tuning(const char *key, int32_t value);
  * (for byte accounting and tests). */
 int32_t td_query_splits(const td_shape *shape, int32_t top_k, int32_t sparse);
 
+/* Which attention kernel the next launch of this shape would run on the
+ * current device with the current tuning: full (sparse = 0; top_k > 0 for a
+ * full+select layer) or sparse (sparse = 1, top_k entries per index row).
+ * Returns a static, NUL-terminated description (the kernel and how it gets
+ * its K/V rows), or "invalid shape".  For reports and tests. */
+const char *td_kernel_name(const td_shape *shape, int32_t top_k, int32_t sparse);
+
 #ifdef __cplusplus
 }
 #endif

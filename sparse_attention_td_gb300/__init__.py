@@ -17,6 +17,6 @@ from ._lib import (  # noqa: F401
     MODE_FULL, MODE_FULL_SELECT, MODE_SPARSE, FLAG_INDEX_OUT_OF_RANGE,
     FLAG_SEQ_LEN_OUT_OF_RANGE, FLAG_WAIT_TIMEOUT, NOALLOC_SCRATCH_BYTES, TdError, Shape, Workspace, Plan, lib, lib_path,
     td_status_string, td_workspace_size, td_workspace_init, td_workspace_status,
-    td_full_attn_select, td_full_attn_select_coverage, td_topk_select, td_index_overlap, td_kv_append, td_probe_layer_reads, td_sparse_attn, td_sparse_attn_noalloc, td_decode_step, td_set_tuning, td_query_splits,
+    td_full_attn_select, td_full_attn_select_coverage, td_topk_select, td_index_overlap, td_kv_append, td_probe_layer_reads, td_sparse_attn, td_sparse_attn_noalloc, td_decode_step, td_set_tuning, td_query_splits, td_kernel_name,
     make_shape, default_scale,
 )

@@ -109,6 +109,8 @@ def lib():
     L.td_set_tuning.argtypes = [ctypes.c_char_p, i32]
     L.td_query_splits.restype = i32
     L.td_query_splits.argtypes = [shp, i32, i32]
+    L.td_kernel_name.restype = ctypes.c_char_p
+    L.td_kernel_name.argtypes = [shp, i32, i32]
     _lib = L
     return L
 
@@ -409,3 +411,7 @@ def td_set_tuning(key: str, value: int):
 
 def td_query_splits(shape: Shape, top_k: int, sparse: bool) -> int:
     return int(lib().td_query_splits(ctypes.byref(shape), int(top_k), int(bool(sparse))))
+
+
+def td_kernel_name(shape: Shape, top_k: int, sparse: bool) -> str:
+    return lib().td_kernel_name(ctypes.byref(shape), int(top_k), int(bool(sparse))).decode()

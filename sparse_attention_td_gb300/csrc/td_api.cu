@@ -981,6 +981,31 @@ td_status td_set_tuning(const char *key, int32_t value)
     return TD_OK;
 }
 
+const char *td_kernel_name(const td_shape *shape, int32_t top_k, int32_t sparse)
+{
+    if (check_shape(shape) != TD_OK || top_k < 0 || top_k > shape->max_seq_len)
+        return "invalid shape";
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const bool sp = sparse != 0;
+    int nsplit = 0, chunk = 0;
+    const long n_total = sp ? top_k : shape->max_seq_len;
+    plan_splits(*shape, n_total, sp, !sp && top_k > 0, nsplit, chunk);
+    if (mma_for(G)) {
+        const int t = mma_tokens_for(sp, chunk);
+        return t == 32   ? "attention_mma16_kernel (tensor cores, 16 tokens per warp, two rounds in flight)"
+               : t == 16 ? "attention_mma16_kernel (tensor cores, 16 tokens per warp)"
+                         : "attention_mma_kernel (tensor cores, 8 tokens per warp)";
+    }
+    if (g_tuning.cluster && nsplit > 1 && nsplit <= td::kPortableClusterSplits)
+        return "attention_kernel (CUDA cores, register-streamed, cluster split merge)";
+    switch (staged_for(*shape, sp, n_total)) {
+    case 2: return "attention_kernel (CUDA cores, TMA row gathers into shared-memory stages)";
+    case 1: return sp ? "attention_kernel (CUDA cores, cp.async rows into shared-memory stages)"
+                      : "attention_kernel (CUDA cores, bulk copies into shared-memory stages)";
+    default: return "attention_kernel (CUDA cores, register-streamed)";
+    }
+}
+
 int32_t td_query_splits(const td_shape *shape, int32_t top_k, int32_t sparse)
 {
     if (check_shape(shape) != TD_OK)

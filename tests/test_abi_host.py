@@ -134,8 +134,17 @@ def test_tuning_keys(L):
     td.td_set_tuning("full_prefetch", -1)
     td.td_set_tuning("topk_warp_max", 2048)
     td.td_set_tuning("topk_warp_max", 0)
+    for key, value in (("mma_full_tokens", 8), ("mma_sparse_tokens", 32), ("topk_cluster", 4),
+                       ("sparse_staged", 2), ("wait_limit_us", 50), ("wait_test", 1)):
+        td.td_set_tuning(key, value)
+        td.td_set_tuning(key, -1 if key not in ("wait_limit_us", "wait_test") else 0)
     with pytest.raises(td.TdError):
         td.td_set_tuning("no_such_knob", 1)
+
+
+def test_kernel_name_of_an_invalid_shape(L):
+    assert td.td_kernel_name(shape(head_dim=64), 0, False) == "invalid shape"
+    assert td.td_kernel_name(shape(), -1, True) == "invalid shape"
 
 
 def test_index_overlap_rejects_bad_arguments(L):
