@@ -44,11 +44,13 @@
 namespace td {
 namespace {
 
+// Not volatile: the compiler may interleave independent MMAs (different
+// accumulators) with each other and with the loads, instead of issuing each
+// right behind the one it depends on.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1)
 {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -194,10 +196,16 @@ attention_mma_kernel(const AttnArgs a)
 
     auto round = [&](int base, const uint2 (&kq)[8], const uint4 (&v0)[2], const uint4 (&v1)[2]) {
         const int tw = base + warp * 8;
-        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // two accumulators (even / odd k-steps): two chains of 4 dependent MMAs
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s_odd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 8; j += 2) {
             mma_bf16(s, kq[j].x, 0u, kq[j].y, 0u, qf[j].x, qf[j].y);
+            mma_bf16(s_odd, kq[j + 1].x, 0u, kq[j + 1].y, 0u, qf[j + 1].x, qf[j + 1].y);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            s[e] += s_odd[e];
         const bool ok = row_of(tw + r) >= 0;
 
         if constexpr (SELECT) {
@@ -258,16 +266,20 @@ attention_mma_kernel(const AttnArgs a)
             pt0 -= __bfloat162float(h0);
             pt1 -= __bfloat162float(h1);
         }
-        // O += V^T P^T, one m-tile of 16 dims at a time
+        // O += V^T P^T, m-tiles of 16 dims; the three terms of P in the
+        // outer loop, so that consecutive MMAs go to different tiles
+        uint32_t lo[8], hi[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t w0 = word2(v0, i), w1 = word2(v1, i);
-            const uint32_t lo = prmt(w0, w1, 0x5410u);  // dim vdim(i) of tokens 2c, 2c+1
-            const uint32_t hi = prmt(w0, w1, 0x7632u);  // dim vdim(i) + 1
-#pragma unroll
-            for (int k = 0; k < 3; ++k)
-                mma_bf16(o[i], lo, hi, 0u, 0u, pb[k], 0u);
+            lo[i] = prmt(w0, w1, 0x5410u);  // dim vdim(i) of tokens 2c, 2c+1
+            hi[i] = prmt(w0, w1, 0x7632u);  // dim vdim(i) + 1
         }
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                mma_bf16(o[i], lo[i], hi[i], 0u, 0u, pb[k], 0u);
     };
 
     if (t0 < t1)
@@ -456,10 +468,16 @@ attention_mma16_kernel(const AttnArgs a)
     auto round = [&](int base, const uint2 (&kq)[2][8], const uint4 (&vv)[4][2]) {
         const int tw = base + warp * 16;
         // s[0], s[1]: token r, heads 2c, 2c+1; s[2], s[3]: token r + 8
-        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s_odd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 8; j += 2) {  // two chains of 4 dependent MMAs
             mma_bf16(s, kq[0][j].x, kq[1][j].x, kq[0][j].y, kq[1][j].y, qf[j].x, qf[j].y);
+            mma_bf16(s_odd, kq[0][j + 1].x, kq[1][j + 1].x, kq[0][j + 1].y, kq[1][j + 1].y,
+                     qf[j + 1].x, qf[j + 1].y);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            s[e] += s_odd[e];
         const bool ok[2] = {row_of(tw + r) >= 0, row_of(tw + r + 8) >= 0};
 
         if constexpr (SELECT) {
@@ -534,16 +552,21 @@ attention_mma16_kernel(const AttnArgs a)
         }
         // O += V^T P^T, one m-tile of 16 dims at a time, k = tokens 2c, 2c+1,
         // 2c+8, 2c+9
+        uint32_t lo[8], hi[8], lo8[8], hi8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t w0 = word2(vv[0], i), w1 = word2(vv[1], i);
             const uint32_t w8 = word2(vv[2], i), w9 = word2(vv[3], i);
-            const uint32_t lo = prmt(w0, w1, 0x5410u), hi = prmt(w0, w1, 0x7632u);
-            const uint32_t lo8 = prmt(w8, w9, 0x5410u), hi8 = prmt(w8, w9, 0x7632u);
-#pragma unroll
-            for (int k = 0; k < 3; ++k)
-                mma_bf16(o[i], lo, hi, lo8, hi8, pb[0][k], pb[1][k]);
+            lo[i] = prmt(w0, w1, 0x5410u);
+            hi[i] = prmt(w0, w1, 0x7632u);
+            lo8[i] = prmt(w8, w9, 0x5410u);
+            hi8[i] = prmt(w8, w9, 0x7632u);
         }
+#pragma unroll
+        for (int k = 0; k < 3; ++k)  // consecutive MMAs go to different tiles
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                mma_bf16(o[i], lo[i], hi[i], lo8[i], hi8[i], pb[0][k], pb[1][k]);
     };
 
     if constexpr (DB) {
