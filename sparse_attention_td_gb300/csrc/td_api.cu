@@ -44,6 +44,8 @@ struct Tuning {
     int topk_cluster = 0;        // CTAs per top-k row of a selection layer: 0 auto, 1, 2, 4, 8
     int pdl = 1;                 // 0: no programmatic dependent launch between a call's kernels
     int topk_pdl = 1;            // 0: the top-k kernel waits for its attention kernel in stream order
+    int sparse_stream_k = 0;     // tensor-core sparse layers: 1 splits the layer's rounds evenly over
+                                 // whole waves of CTAs (stream-K), 0 one CTA per split
     int mma_full_tokens = 16;    // tensor-core full / full+select kernels: tokens per warp per round
     int mma_sparse_tokens = 0;   // tensor-core sparse kernels: tokens per warp per round (8, 16, or
                                  // 32 = 16 with two rounds in flight); 0: 32 when a CTA's chunk
@@ -479,6 +481,43 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
 
 // idx_dep: the kernel launched just before may have written `idx` (then the
 // sparse kernel waits for it before reading the set).
+// Stream-K plan of a tensor-core sparse launch (16 tokens per warp): whole
+// waves of CTAs share the layer's B * Hkv * R rounds evenly, at most
+// kMaxSparseChunk index entries per CTA; two rounds in flight per warp when
+// the CTAs get 16 rounds or more.  a.nsplit becomes the partial stride: the
+// largest number of CTAs that meet one (batch row, KV head).  False (plan
+// unchanged) when the workspace's partials cannot hold them.
+bool plan_stream_k(const Ctx &c, int top_k, td::AttnArgs &a, int &tokens)
+{
+    const long units = (long)c.shape.batch * c.shape.num_kv_heads;
+    if (top_k < 1 || units > (1L << 16))
+        return false;
+    const long R = ceil_div(top_k, td::kTokPerRound);
+    const long W = units * R;
+    const long sms = device_sm_count();
+    const long slots32 = sms * td::attention_mma_ctas_per_sm(c.G, true, false, 32);
+    const bool db = W >= slots32 * 16;
+    tokens = db ? 32 : 16;
+    const long slots = db ? slots32 : sms * td::attention_mma_ctas_per_sm(c.G, true, false, 16);
+    const long cap = td::kMaxSparseChunk / td::kTokPerRound;  // rounds one CTA stages
+    const long waves = ceil_div(W, slots * cap);
+    long P = slots * (waves > 0 ? waves : 1);
+    if (P > W)
+        P = W;
+    long most = 1;  // CTAs meeting one (batch row, KV head); CTA of round y: ((y+1)P-1)/W
+    for (long u = 0; u < units; ++u) {
+        const long pf = ((u * R + 1) * P - 1) / W, pl = ((u + 1) * R * P - 1) / W;
+        if (pl - pf + 1 > most)
+            most = pl - pf + 1;
+    }
+    if (units * most > partial_slots(c.shape, top_k))
+        return false;
+    a.sk_ctas = (int)P;
+    a.sk_units = (int)units;
+    a.nsplit = (int)most;
+    return true;
+}
+
 td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
                      const int32_t *seq_lens, const int32_t *idx, int top_k, void *out,
                      float *out_f32, cudaStream_t st, bool idx_dep, bool pdl)
@@ -490,6 +529,13 @@ td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
     plan_splits(c.shape, top_k, true, false, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;
     const int staged = staged_for(c.shape, true, top_k);
+    int sk_tokens = 0;
+    if (mma_for(c.G) && g_tuning.sparse_stream_k > 0 && plan_stream_k(c, top_k, a, sk_tokens)) {
+        if (td::launch_attention_mma(c.G, true, false, sk_tokens, a, c.shape.batch, pdl, st) !=
+            cudaSuccess)
+            return TD_ERR_CUDA;
+        return TD_OK;
+    }
     if (!mma_for(c.G) && !cluster && staged == 2) {
         const long rows = (long)c.shape.batch * c.shape.num_kv_heads * c.shape.max_seq_len;
         if (!encode_row_map(&a.tma_k, k, rows) || !encode_row_map(&a.tma_v, v, rows))
@@ -956,6 +1002,8 @@ td_status td_set_tuning(const char *key, int32_t value)
         g_tuning.pdl = value != 0 ? 1 : 0;
     else if (!strcmp(key, "topk_pdl"))
         g_tuning.topk_pdl = value != 0 ? 1 : 0;
+    else if (!strcmp(key, "sparse_stream_k"))
+        g_tuning.sparse_stream_k = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.sparse_stream_k);
     else if (!strcmp(key, "mma_full_tokens"))
         g_tuning.mma_full_tokens =
             (value == 8 || value == 16 || value == 32) ? value : kDefaultTuning.mma_full_tokens;
@@ -991,6 +1039,8 @@ const char *td_kernel_name(const td_shape *shape, int32_t top_k, int32_t sparse)
     const long n_total = sp ? top_k : shape->max_seq_len;
     plan_splits(*shape, n_total, sp, !sp && top_k > 0, nsplit, chunk);
     if (mma_for(G)) {
+        if (sp && g_tuning.sparse_stream_k > 0)
+            return "attention_mma16_kernel (tensor cores, 16 tokens per warp, stream-K partition)";
         const int t = mma_tokens_for(sp, chunk);
         return t == 32   ? "attention_mma16_kernel (tensor cores, 16 tokens per warp, two rounds in flight)"
                : t == 16 ? "attention_mma16_kernel (tensor cores, 16 tokens per warp)"

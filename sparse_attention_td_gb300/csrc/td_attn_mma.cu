@@ -350,11 +350,19 @@ attention_mma_kernel(const AttnArgs a)
 constexpr int kMma16Warps = kTokPerRound / 16;
 constexpr int kMma16Threads = kMma16Warps * 32;
 
-template <int G, bool SPARSE, bool SELECT, bool DB>
+// SK (sparse only): stream-K partition of the launch.  The grid is 1D; the
+// layer's B * Hkv * R rounds (R = rounds of 64 index entries per (batch row,
+// KV head)) are split evenly over the CTAs, so every CTA gets the same number
+// of rounds and a CTA's range may cover the end of one (batch row, KV head)
+// and the start of the next.  It publishes one partial per (batch row, KV
+// head) it touched; the split merge counts, per (batch row, KV head), the CTAs
+// whose ranges meet it.  Without SK: one CTA per (split, KV head, batch row).
+template <int G, bool SPARSE, bool SELECT, bool DB, bool SK = false>
 __global__ void __launch_bounds__(kMma16Threads, DB ? 2 : 3)
 attention_mma16_kernel(const AttnArgs a)
 {
     static_assert(G == 4 || G == 8, "heads of a group are the MMA's N = 8 columns");
+    static_assert(!SK || SPARSE, "the stream-K partition serves sparse layers");
     constexpr int NW = kMma16Warps, NT = kMma16Threads;
     __shared__ float sm_m[NW][G];
     __shared__ float sm_l[NW][G];
@@ -366,9 +374,42 @@ attention_mma16_kernel(const AttnArgs a)
     __shared__ int sm_last;
     __shared__ unsigned sm_hist[SELECT ? kSelectBins : 1];
 
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = lane >> 2, c = lane & 3;  // MMA fragment row group / quad position
+
+    // SK: this CTA's rounds [x, x_end) of the layer's W rounds, R per (batch
+    // row, KV head); CTA p covers [floor(p W / P), floor((p + 1) W / P)).
+    const long R = SK ? (a.top_k + kTokPerRound - 1) / kTokPerRound : 1;
+    const long W = SK ? (long)a.sk_units * R : 1;
+    const long P = SK ? gridDim.x : 1;
+    long x = SK ? (long)blockIdx.x * W / P : 0;
+    const long x_end = SK ? ((long)blockIdx.x + 1) * W / P : 1;
+    for (bool first = true; x < x_end; first = false) {
+    int split, g, b, t0, t1, nsplit_b;
+    if constexpr (SK) {
+        // the (batch row, KV head) u of round x, the CTAs meeting it, and this
+        // CTA's place among them (the CTA holding round y is
+        // floor(((y + 1) P - 1) / W))
+        const long u = x / R;
+        const long seg_end = min(x_end, (u + 1) * R);
+        const long p_first = ((u * R + 1) * P - 1) / W;
+        const long p_last = ((u + 1) * R * P - 1) / W;
+        split = (int)(blockIdx.x - p_first);
+        nsplit_b = (int)(p_last - p_first + 1);
+        b = (int)(u / a.Hkv);
+        g = (int)(u % a.Hkv);
+        t0 = (int)((x - u * R) * kTokPerRound);
+        t1 = min((int)((seg_end - u * R) * kTokPerRound), a.top_k);
+        x = seg_end;
+        if (!first)
+            __syncthreads();  // the previous segment is done with shared memory
+    } else {
+        split = blockIdx.x;
+        g = blockIdx.y;
+        b = blockIdx.z;
+        x = x_end;
+    }
+    (void)first;
 
     int n_b = a.seq_lens[b];
     if (n_b < 0 || n_b > a.Nmax) {
@@ -376,12 +417,14 @@ attention_mma16_kernel(const AttnArgs a)
             atomicOr(a.status, kFlagSeqLenOutOfRange);
         n_b = n_b < 0 ? 0 : a.Nmax;
     }
-    const int n_total = SPARSE ? a.top_k : n_b;
-    const int nsplit_b = n_total > 0 ? (n_total + a.chunk - 1) / a.chunk : 1;
-    if (split >= nsplit_b)
-        return;
-    const int t0 = split * a.chunk;
-    const int t1 = min(t0 + a.chunk, n_total);
+    if constexpr (!SK) {
+        const int n_total = SPARSE ? a.top_k : n_b;
+        nsplit_b = n_total > 0 ? (n_total + a.chunk - 1) / a.chunk : 1;
+        if (split >= nsplit_b)
+            return;
+        t0 = split * a.chunk;
+        t1 = min(t0 + a.chunk, n_total);
+    }
     const size_t bg = (size_t)b * a.Hkv + g;
     const uint16_t *kbase = a.k + bg * (size_t)a.Nmax * kHeadDim;
     const uint16_t *vbase = a.v + bg * (size_t)a.Nmax * kHeadDim;
@@ -638,6 +681,7 @@ attention_mma16_kernel(const AttnArgs a)
     __syncthreads();
     const size_t out_row0 = (size_t)b * a.Hq + (size_t)g * G;
     finish_splits<G, NW, NT>(a, sm_o, sm_w, sm_M, sm_L, &sm_last, bg, split, nsplit_b, out_row0);
+    }  // segments
 }
 
 template <typename Kern>
@@ -667,9 +711,29 @@ int occupancy(Kern kern, int threads)
 
 // tokens: 8 (attention_mma_kernel), 16 (attention_mma16_kernel, one round in
 // flight per warp) or 32 (attention_mma16_kernel, two rounds in flight).
+// a.sk_ctas > 0 (sparse, tokens 16 or 32): the stream-K partition over a 1D
+// grid of a.sk_ctas CTAs for a.sk_units (batch row, KV head) pairs (partials
+// with a stride of a.nsplit per pair).
 template <int G, bool SPARSE, bool SELECT>
 cudaError_t launch_mma_one(int tokens, const AttnArgs &a, int batch, bool pdl, cudaStream_t st)
 {
+    if constexpr (SPARSE) {
+        if (a.sk_ctas > 0) {
+            const AttnArgs &sk = a;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)a.sk_ctas);
+            cfg.blockDim = dim3(kMma16Threads);
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return tokens == 32
+                       ? cudaLaunchKernelEx(&cfg, attention_mma16_kernel<G, true, false, true, true>, sk)
+                       : cudaLaunchKernelEx(&cfg, attention_mma16_kernel<G, true, false, false, true>, sk);
+        }
+    }
     if (tokens == 32)
         return launch_kernel(attention_mma16_kernel<G, SPARSE, SELECT, true>, kMma16Threads, a,
                              batch, pdl, st);

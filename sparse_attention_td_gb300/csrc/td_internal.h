@@ -60,6 +60,9 @@ struct AttnArgs {
     int wait_test;           // staged full layers: each CTA's first wait polls a barrier nothing
                              // arrives on (tests of the failure report); 0 in normal use
     float scale;             // softmax scale (natural-log units)
+    int sk_ctas;             // sparse, stream-K partition (tensor cores, 16 tokens per warp): the
+                             // CTAs (1D grid) sharing the layer's rounds evenly; 0: not used
+    int sk_units;            // with sk_ctas: (batch row, KV head) pairs, B * Hkv
     int tma_rows;            // sparse, row gathers: rows of the maps (B * Hkv * Nmax)
     TmaDesc tma_k, tma_v;    // sparse, row gathers: maps over the K / V cache rows
 };

@@ -47,8 +47,10 @@ NON_DEFAULT_PATHS = {
     "prefetch2": {"mma": 1, "full_prefetch": 2},
     "mma8": {"mma_full_tokens": 8},
     "mma16": {"mma_sparse_tokens": 16},
+    "stream_k": {"sparse_stream_k": 1},
 }
-PATH_CASES = [(p, "llama3-8b-32k") for p in NON_DEFAULT_PATHS] + [("tma", "llama2-7b-100k")]
+PATH_CASES = [(p, "llama3-8b-32k") for p in NON_DEFAULT_PATHS] + [("tma", "llama2-7b-100k"),
+                                                                   ("stream_k", "serving-b32")]
 
 
 @pytest.mark.parametrize("name,k,n_groups", CASES, ids=[f"{c[0]}-k{c[1]}" for c in CASES])
@@ -64,7 +66,7 @@ def test_full_size_step_on_non_default_kernel_paths(path, workload):
         _step_against_oracle(workload, None, 3)
     finally:
         for key in ("mma", "full_staged", "sparse_staged", "full_prefetch", "mma_full_tokens",
-                    "mma_sparse_tokens"):
+                    "mma_sparse_tokens", "sparse_stream_k"):
             td.td_set_tuning(key, -1)
 
 
