@@ -316,9 +316,11 @@ __device__ __forceinline__ int topk_row_budget(const TopkArgs &a, size_t bg)
 
 // The whole selection of row (b, KV head g) by one CTA of NT threads, with
 // the dynamic shared memory of topk_kernel<NT>.  Called after the wait for
-// the kernel that wrote the scores.
+// the kernel that wrote the scores.  Not inlined: the clustered kernel calls
+// it only for the rows it cannot take, and keeping its code out of that
+// kernel's body keeps the common path small.
 template <int NT>
-__device__ void topk_row(const TopkArgs &a, int g, int b, unsigned char *smem_raw)
+__device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned char *smem_raw)
 {
     using C = TopkCfg<NT>;
     constexpr int kT = C::kT, kWarps = C::kWarps, kWordsPerThread = C::kWordsPerThread;
