@@ -26,7 +26,7 @@
  *   - a coverage budget for the selection (Token Sparse Attention page, §2
  *     "Dynamic Token Coverage").
  *
- * Readings where the page is silent (each also listed in the design notes):
+ * Readings where the page is silent:
  *   - "attention score" for selection is the scaled pre-softmax logit a;
  *   - with grouped-query attention the score of a KV head is the sum of the
  *     scaled logits of the query heads in its group;

@@ -14,9 +14,9 @@
 //     r + 8 of S are two tokens, the P V k-step takes all 16), a CTA of 4
 //     warps 64 tokens; half the MMAs and shuffles per token, 3 CTAs per SM.
 //     Default for full and full+select layers.
-// Measured on GB300 (design notes): the 16-token kernel takes 2-6% off full
-// and full+select layers, but is slower on sparse layers, whose CTAs are
-// short and latency-bound; there the 8-token kernel stays.  The splits of
+// Measured on GB300: the 16-token kernel takes 2-6% off full and full+select
+// layers, but is slower on sparse layers whose CTAs are short and
+// latency-bound; there the 8-token kernel stays.  The splits of
 // either merge as in the CUDA-core kernels.
 //
 // Fragments come straight from global memory.  The dot product does not care
