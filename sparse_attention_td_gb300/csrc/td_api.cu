@@ -329,8 +329,13 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
     }
     const long slots = (long)device_sm_count() * per_sm;  // resident CTAs per wave
     int waves = sparse ? g_tuning.sparse_waves : g_tuning.full_waves;
-    if (waves <= 0)  // one wave of long CTAs when the pairs are few; more, shorter
-        waves = units * 2 <= slots ? 1 : 3;  // CTAs balance ragged lengths otherwise
+    // One wave of long CTAs when the pairs are few; more, shorter CTAs balance
+    // ragged lengths otherwise.  Measured on GB300 (serving batch, 256 pairs of
+    // 8K-16K tokens): 3 waves best for the CUDA-core kernels; 4 for the
+    // tensor-core full kernels (full layer 253.6 -> 241.1 us, step -3%; 2 and
+    // 6 waves slower).
+    if (waves <= 0)
+        waves = units * 2 <= slots ? 1 : (mma_for(G) && !sparse ? 4 : 3);
     const long target = slots * waves;
     const int cap = split_cap(units, n_total, sparse);
     long want = target / units;  // whole waves: never spill a few CTAs into an extra wave
