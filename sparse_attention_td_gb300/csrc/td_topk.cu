@@ -66,6 +66,8 @@ struct TopkCfg {
     static constexpr int kMinBlocks = 1024 / NT;
 };
 
+constexpr int kShortList = 256;         // pairs one warp finishes after the second digit
+
 template <int NT>
 struct TopkSmem {
     static constexpr int kWarps = NT / 32;
@@ -75,7 +77,10 @@ struct TopkSmem {
     unsigned pre[kBatch * kWarps];
     unsigned res[2];                    // digit, remaining rank
     unsigned cand_count;
-    unsigned cut[2];                    // cluster path: the k-th key T and the largest kept position P
+    unsigned cut[2];                    // the k-th key T and the largest kept position P
+    unsigned short_count;               // pairs of the narrowed threshold bin
+    uint32_t short_key[kShortList];     // the narrowed bin's pairs (bin_cut)
+    int32_t short_pos[kShortList];
     unsigned slice_total;               // cluster path: positions this CTA's slice keeps
     unsigned bitmap[kBitmapWords];      // selected positions of rows up to kTopkBitmapBits long
 };
@@ -290,6 +295,113 @@ __device__ uint32_t warp_select(unsigned *hist, unsigned n, ValF val, KeepF keep
     return prefix;
 }
 
+// The cut of a threshold bin whose cnt (key, position) pairs are in shared
+// memory (keys share prefix1 under mask1): T = the r1-th largest key, P = the
+// largest position kept among keys equal to T (lower positions win ties;
+// INT_MAX when every key equal to T is kept).  A bin of up to warp_max pairs
+// is finished by one warp.  A larger one is narrowed first: its pairs' next
+// 8-bit digit is counted, the digit holding the r1-th key found, and that
+// digit's pairs (a few, unless the keys are heavily tied) are copied to a
+// short list that one warp finishes; a digit with more than kShortList pairs
+// takes block-wide radix passes over the bin.  All threads call it; the cut
+// is in sm.cut on return.
+template <int NT>
+__device__ void bin_cut(TopkSmem<NT> &sm, const uint32_t *cand_key, const int32_t *cand_pos,
+                        unsigned cnt, uint32_t prefix1, uint32_t mask1, unsigned r1,
+                        unsigned warp_max)
+{
+    constexpr int kT = NT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (cnt <= warp_max) {
+        if (warp == 0) {
+            unsigned need, neq;
+            const uint32_t t = warp_select(
+                sm.hist, cnt, [&](unsigned i) { return cand_key[i]; },
+                [&](unsigned) { return true; }, 31 - kBits1, prefix1, mask1, r1, &need, &neq);
+            int p_cut = 0x7fffffff;
+            if (need < neq) {
+                unsigned r2, e2;
+                p_cut = (int)~warp_select(
+                    sm.hist, cnt, [&](unsigned i) { return ~(uint32_t)cand_pos[i]; },
+                    [&](unsigned i) { return cand_key[i] == t; }, 31, 0u, 0u, need, &r2, &e2);
+            }
+            if (lane == 0) {
+                sm.cut[0] = t;
+                sm.cut[1] = (unsigned)p_cut;
+            }
+        }
+        __syncthreads();
+        return;
+    }
+    // second digit: key bits 20..13
+    constexpr int kShift2 = 32 - kBits1 - 8;
+    for (int i = tid; i < 256; i += kT)
+        sm.hist[i] = 0u;
+    if (tid == 0)
+        sm.short_count = 0u;
+    __syncthreads();
+    for (unsigned i = tid; i < cnt; i += kT)
+        atomicAdd(&sm.hist[(cand_key[i] >> kShift2) & 0xffu], 1u);
+    __syncthreads();
+    find_digit<256>(sm, sm.hist, r1);
+    const uint32_t d2 = sm.res[0];
+    const unsigned r2 = sm.res[1];
+    const unsigned n2 = sm.hist[d2];
+    const uint32_t prefix2 = prefix1 | (d2 << kShift2);
+    const uint32_t mask2 = mask1 | (0xffu << kShift2);
+    __syncthreads();
+    if (n2 <= (unsigned)kShortList) {
+        for (unsigned i = tid; i < cnt; i += kT)
+            if ((cand_key[i] & mask2) == prefix2) {
+                const unsigned slot = atomicAdd(&sm.short_count, 1u);  // n2 slots in all
+                sm.short_key[slot] = cand_key[i];
+                sm.short_pos[slot] = cand_pos[i];
+            }
+        __syncthreads();
+        if (warp == 0) {
+            unsigned need, neq;
+            const uint32_t t = warp_select(
+                sm.hist, n2, [&](unsigned i) { return sm.short_key[i]; },
+                [&](unsigned) { return true; }, kShift2 - 1, prefix2, mask2, r2, &need, &neq);
+            int p_cut = 0x7fffffff;
+            if (need < neq) {
+                unsigned rr, ee;
+                p_cut = (int)~warp_select(
+                    sm.hist, n2, [&](unsigned i) { return ~(uint32_t)sm.short_pos[i]; },
+                    [&](unsigned i) { return sm.short_key[i] == t; }, 31, 0u, 0u, need, &rr, &ee);
+            }
+            if (lane == 0) {
+                sm.cut[0] = t;
+                sm.cut[1] = (unsigned)p_cut;
+            }
+        }
+        __syncthreads();
+        return;
+    }
+    // heavily tied: block-wide radix passes over the bin's remaining digits
+    auto cand_src = [&](auto f) {
+        for (unsigned i = tid; i < cnt; i += kT)
+            f(cand_key[i], cand_pos[i]);
+    };
+    unsigned need_eq, n_eq;
+    const uint32_t T = radix_select(sm, cand_src, kShift2 - 1, prefix2, mask2, r2, &need_eq, &n_eq);
+    int P = 0x7fffffff;
+    if (need_eq < n_eq) {
+        auto eq_src = [&](auto f) {
+            for (unsigned i = tid; i < cnt; i += kT)
+                if (cand_key[i] == T)
+                    f(~(uint32_t)cand_pos[i], 0);
+        };
+        unsigned r_dummy, e_dummy;
+        P = (int)~radix_select(sm, eq_src, 31, 0u, 0u, need_eq, &r_dummy, &e_dummy);
+    }
+    if (tid == 0) {
+        sm.cut[0] = T;
+        sm.cut[1] = (unsigned)P;
+    }
+    __syncthreads();
+}
+
 // Row length n of batch row b (clamped to [0, Nmax]; out-of-range lengths
 // are flagged once per batch row by `flag`).
 __device__ __forceinline__ int topk_row_len(const TopkArgs &a, int b, bool flag)
@@ -478,45 +590,9 @@ __device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned 
         __syncthreads();
         const unsigned cnt = sm.cand_count;
         const unsigned warp_max = a.warp_select_max > 0 ? (unsigned)a.warp_select_max : kWarpSelectMax;
-        if (use_bitmap && cnt <= warp_max) {
-            // small threshold bin: one warp finishes the select and marks the
-            // selected candidates, without block-wide barriers
-            if (warp == 0) {
-                unsigned need, neq;
-                const uint32_t t = warp_select(
-                    sm.hist, cnt, [&](unsigned i) { return cand_key[i]; },
-                    [&](unsigned) { return true; }, 31 - kBits1, prefix1, mask1, r1, &need, &neq);
-                int p_cut = 0x7fffffff;
-                if (need < neq) {
-                    unsigned r2, e2;
-                    p_cut = (int)~warp_select(
-                        sm.hist, cnt, [&](unsigned i) { return ~(uint32_t)cand_pos[i]; },
-                        [&](unsigned i) { return cand_key[i] == t; }, 31, 0u, 0u, need, &r2, &e2);
-                }
-                for (unsigned i = lane; i < cnt; i += 32) {
-                    const uint32_t key = cand_key[i];
-                    const int pos = cand_pos[i];
-                    if (key > t || (key == t && pos <= p_cut))
-                        atomicOr(&sm.bitmap[pos >> 5], 1u << (pos & 31));
-                }
-            }
-            __syncthreads();
-        } else {
-        auto cand_src = [&](auto f) {
-            for (unsigned i = tid; i < cnt; i += kT)
-                f(cand_key[i], cand_pos[i]);
-        };
-        T = radix_select(sm, cand_src, 31 - kBits1, prefix1, mask1, r1, &need_eq, &n_eq);
-        if (need_eq < n_eq) {
-            // lowest positions win: the need_eq-th largest of ~pos among keys == T
-            auto eq_src = [&](auto f) {
-                for (unsigned i = tid; i < cnt; i += kT)
-                    if (cand_key[i] == T)
-                        f(~(uint32_t)cand_pos[i], 0);
-            };
-            unsigned r_dummy, e_dummy;
-            P = (int)~radix_select(sm, eq_src, 31, 0u, 0u, need_eq, &r_dummy, &e_dummy);
-        }
+        bin_cut<NT>(sm, cand_key, cand_pos, cnt, prefix1, mask1, r1, warp_max);
+        T = sm.cut[0];
+        P = (int)sm.cut[1];
         if (use_bitmap) {
             // mark the selected part of the threshold bin
             for (unsigned i = tid; i < cnt; i += kT) {
@@ -527,7 +603,6 @@ __device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned 
             }
             __syncthreads();
         }
-        }  // large threshold bin
         if (use_bitmap) {
             // write the set in position order by scanning the bitmap (no second row read)
             const int words = (n + 31) / 32;
@@ -834,48 +909,9 @@ topk_cluster_kernel(const TopkArgs a)
             total += cnt;
         }
         __syncthreads();
-        uint32_t T;
-        int P = 0x7fffffff;
         const unsigned warp_max =
             a.warp_select_max > 0 ? (unsigned)a.warp_select_max : kWarpSelectMax;
-        if (total <= warp_max) {
-            if (warp == 0) {
-                unsigned need, neq;
-                T = warp_select(
-                    sm.hist, total, [&](unsigned i) { return cand_key[i]; },
-                    [&](unsigned) { return true; }, 31 - kBits1, prefix1, mask1, r1, &need, &neq);
-                if (need < neq) {
-                    unsigned r2, e2;
-                    P = (int)~warp_select(
-                        sm.hist, total, [&](unsigned i) { return ~(uint32_t)cand_pos[i]; },
-                        [&](unsigned i) { return cand_key[i] == T; }, 31, 0u, 0u, need, &r2, &e2);
-                }
-                if (lane == 0) {
-                    sm.cut[0] = T;
-                    sm.cut[1] = (unsigned)P;
-                }
-            }
-        } else {
-            auto cand_src = [&](auto f) {
-                for (unsigned i = tid; i < total; i += kT)
-                    f(cand_key[i], cand_pos[i]);
-            };
-            unsigned need_eq, n_eq;
-            T = radix_select(sm, cand_src, 31 - kBits1, prefix1, mask1, r1, &need_eq, &n_eq);
-            if (need_eq < n_eq) {
-                auto eq_src = [&](auto f) {
-                    for (unsigned i = tid; i < total; i += kT)
-                        if (cand_key[i] == T)
-                            f(~(uint32_t)cand_pos[i], 0);
-                };
-                unsigned r_dummy, e_dummy;
-                P = (int)~radix_select(sm, eq_src, 31, 0u, 0u, need_eq, &r_dummy, &e_dummy);
-            }
-            if (tid == 0) {
-                sm.cut[0] = T;
-                sm.cut[1] = (unsigned)P;
-            }
-        }
+        bin_cut<NT>(sm, cand_key, cand_pos, total, prefix1, mask1, r1, warp_max);
     }
     cluster.sync();  // the cut is in rank 0's shared memory; rank 0 is done reading the pairs
     const uint32_t T = *cluster.map_shared_rank(&sm.cut[0], 0);
