@@ -72,6 +72,7 @@ template <int NT>
 struct TopkSmem {
     static constexpr int kWarps = NT / 32;
     unsigned hist[kBins1];              // first-digit histogram, later a 256-bin scratch histogram
+    unsigned hist2[256];                // second digit (key bits 20..13) of the threshold bin's pairs
     unsigned scan[32];                  // per-warp partial sums (entries >= kWarps stay unused)
     unsigned tot[kBatch * kWarps];
     unsigned pre[kBatch * kWarps];
@@ -227,6 +228,45 @@ __device__ uint32_t radix_select(TopkSmem<NT> &sm, Src src, int hi_bit, uint32_t
     return prefix;
 }
 
+// One warp's search of a 256-bin histogram, lane L holding bins 255 - 8L down
+// to 248 - 8L: the digit d with count(> d) < r <= count(>= d).  Returns d to
+// every lane; *rank_out = r - count(> d), *cnt_out = count(d).
+__device__ __forceinline__ uint32_t warp_find_digit(const unsigned *hist, unsigned r,
+                                                    unsigned *rank_out, unsigned *cnt_out)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned mine = 0;
+    for (int i = 0; i < 8; ++i)
+        mine += hist[255 - 8 * lane - i];
+    unsigned incl = mine;
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned t = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off)
+            incl += t;
+    }
+    const unsigned excl = incl - mine;
+    const bool owner = excl < r && r <= incl;
+    unsigned d = 0, rn = 0, cnt = 0;
+    if (owner) {
+        unsigned run = excl;
+        for (int i = 0; i < 8; ++i) {
+            const unsigned bin = 255 - 8 * lane - i;
+            const unsigned h = hist[bin];
+            if (run + h >= r) {
+                d = bin;
+                rn = r - run;
+                cnt = h;
+                break;
+            }
+            run += h;
+        }
+    }
+    const int src = __ffs(__ballot_sync(kFull, owner)) - 1;
+    *rank_out = __shfl_sync(kFull, rn, src);
+    *cnt_out = __shfl_sync(kFull, cnt, src);
+    return __shfl_sync(kFull, d, src);
+}
+
 // One warp's radix select over n items of a shared-memory list: the r-th
 // largest value val(i) among the items with keep(i), digits of 8 bits over
 // bits [hi_bit..0] below the already fixed `prefix`/`mask`.  `hist` is a
@@ -255,37 +295,9 @@ __device__ uint32_t warp_select(unsigned *hist, unsigned n, ValF val, KeepF keep
                 atomicAdd(&hist[(v >> shift) & dmask], 1u);
         }
         __syncwarp();
-        // lane L owns bins 255-8L down to 248-8L; counts accumulate from the top
-        unsigned mine = 0;
-        for (int i = 0; i < 8; ++i)
-            mine += hist[255 - 8 * lane - i];
-        unsigned incl = mine;
-        for (int off = 1; off < 32; off <<= 1) {
-            const unsigned t = __shfl_up_sync(kFull, incl, off);
-            if (lane >= off)
-                incl += t;
-        }
-        const unsigned excl = incl - mine;
-        const bool owner = excl < r && r <= incl;
-        unsigned d = 0, rn = 0, cnt = 0;
-        if (owner) {
-            unsigned run = excl;
-            for (int i = 0; i < 8; ++i) {
-                const unsigned bin = 255 - 8 * lane - i;
-                const unsigned h = hist[bin];
-                if (run + h >= r) {
-                    d = bin;
-                    rn = r - run;
-                    cnt = h;
-                    break;
-                }
-                run += h;
-            }
-        }
-        const int src = __ffs(__ballot_sync(kFull, owner)) - 1;
-        d = __shfl_sync(kFull, d, src);
-        r = __shfl_sync(kFull, rn, src);
-        last = __shfl_sync(kFull, cnt, src);
+        unsigned rn;
+        const uint32_t d = warp_find_digit(hist, r, &rn, &last);
+        r = rn;
         prefix |= d << shift;
         mask |= dmask << shift;
         __syncwarp();
@@ -299,12 +311,14 @@ __device__ uint32_t warp_select(unsigned *hist, unsigned n, ValF val, KeepF keep
 // memory (keys share prefix1 under mask1): T = the r1-th largest key, P = the
 // largest position kept among keys equal to T (lower positions win ties;
 // INT_MAX when every key equal to T is kept).  A bin of up to warp_max pairs
-// is finished by one warp.  A larger one is narrowed first: its pairs' next
-// 8-bit digit is counted, the digit holding the r1-th key found, and that
-// digit's pairs (a few, unless the keys are heavily tied) are copied to a
-// short list that one warp finishes; a digit with more than kShortList pairs
-// takes block-wide radix passes over the bin.  All threads call it; the cut
-// is in sm.cut on return.
+// is finished by one warp.  A larger one is narrowed first by its pairs' next
+// 8-bit digit (key bits 20..13), whose counts the caller's row pass left in
+// sm.hist2 (visible to every thread on entry): every warp finds
+// the digit holding the r1-th key, the block copies that digit's pairs (a
+// few, unless the keys are heavily tied) to a short list, and one warp
+// finishes there; a digit with more than kShortList pairs takes block-wide
+// radix passes over the bin.  sm.short_count is zero on entry.  All threads
+// call it; the cut is in sm.cut on return.
 template <int NT>
 __device__ void bin_cut(TopkSmem<NT> &sm, const uint32_t *cand_key, const int32_t *cand_pos,
                         unsigned cnt, uint32_t prefix1, uint32_t mask1, unsigned r1,
@@ -335,21 +349,11 @@ __device__ void bin_cut(TopkSmem<NT> &sm, const uint32_t *cand_key, const int32_
     }
     // second digit: key bits 20..13
     constexpr int kShift2 = 32 - kBits1 - 8;
-    for (int i = tid; i < 256; i += kT)
-        sm.hist[i] = 0u;
-    if (tid == 0)
-        sm.short_count = 0u;
-    __syncthreads();
-    for (unsigned i = tid; i < cnt; i += kT)
-        atomicAdd(&sm.hist[(cand_key[i] >> kShift2) & 0xffu], 1u);
-    __syncthreads();
-    find_digit<256>(sm, sm.hist, r1);
-    const uint32_t d2 = sm.res[0];
-    const unsigned r2 = sm.res[1];
-    const unsigned n2 = sm.hist[d2];
+    // every warp finds the digit holding the r1-th key (no block barrier)
+    unsigned r2, n2;
+    const uint32_t d2 = warp_find_digit(sm.hist2, r1, &r2, &n2);
     const uint32_t prefix2 = prefix1 | (d2 << kShift2);
     const uint32_t mask2 = mask1 | (0xffu << kShift2);
-    __syncthreads();
     if (n2 <= (unsigned)kShortList) {
         for (unsigned i = tid; i < cnt; i += kT)
             if ((cand_key[i] & mask2) == prefix2) {
@@ -461,11 +465,28 @@ __device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned 
         return;
     }
 
+    const int vec_n = (((uintptr_t)s & 15u) == 0) ? n / 4 : 0;  // whole float4 groups
+    const bool use_bitmap = n <= kTopkBitmapBits;
+    // The first batch of the row's float4 groups, requested before the
+    // first-digit search it waits for (the row pass below starts with it).
+    float4 v[kBatchV];
+    auto load_batch = [&](int base) {
+#pragma unroll
+        for (int j = 0; j < kBatchV; ++j) {
+            const int i4 = base + j * kT + tid;
+            v[j] = i4 < vec_n ? __ldcg(reinterpret_cast<const float4 *>(s) + i4)
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+    };
+
     // 1. histogram of the top 11 bits: from the attention kernel that wrote
     //    the scores (then cleared for the next selection), else counted here
-    if (tid == 0)
+    if (tid == 0) {
         sm.cand_count = 0u;
+        sm.short_count = 0u;
+    }
     if (ghist) {
+        load_batch(0);
         for (int i = tid; i < kBins1; i += kT) {
             sm.hist[i] = __ldcg(&ghist[i]);
             ghist[i] = 0u;
@@ -485,7 +506,14 @@ __device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned 
                 t += sub[h * kBins1 + i];
             sm.hist[i] = t;
         }
+        load_batch(0);
     }
+    // the bitmap and the second-digit counts start empty
+    if (use_bitmap)
+        for (int w = tid; w < (n + 31) / 32; w += kT)
+            sm.bitmap[w] = 0u;
+    for (int i = tid; i < 256; i += kT)
+        sm.hist2[i] = 0u;
     __syncthreads();
     find_digit<kBins1>(sm, sm.hist, (unsigned)k);
     const uint32_t d1 = sm.res[0];
@@ -498,31 +526,21 @@ __device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned 
     uint32_t T;
     unsigned need_eq, n_eq;
     int P = 0x7fffffff;  // largest kept position among keys == T
-    const bool use_bitmap = n <= kTopkBitmapBits;
+    constexpr int kShift2 = 32 - kBits1 - 8;  // second digit: key bits 20..13
     if (bin_count <= (unsigned)C::kCand) {
         // 2. gather the threshold bin into shared memory, finish there; rows
         //    that fit the bitmap also mark every key above the bin as selected
-        if (use_bitmap) {
-            for (int w = tid; w < (n + 31) / 32; w += kT)
-                sm.bitmap[w] = 0u;
-            __syncthreads();
-        }
         const uint32_t top_of_bin = prefix1 | ~mask1;  // largest key inside the threshold bin
-        const int vec_n = (((uintptr_t)s & 15u) == 0) ? n / 4 : 0;  // whole float4 groups
         // Aligned rows: a thread takes 4 consecutive scores per load, so a warp
         // covers 128 positions = 4 bitmap words (a word's 8 nibbles are OR-ed
         // together with 3 shuffles).  A key is in the threshold bin (above it)
         // when its first digit equals (exceeds) d1.  The bin holds a few
         // percent of the row at most, so each hit takes its candidate slot
-        // with its own shared-memory atomic: no per-group warp scan.
+        // with its own shared-memory atomic (no per-group warp scan) and
+        // counts its second digit.
         for (int base = 0; base < vec_n; base += kT * kBatchV) {
-            float4 v[kBatchV];
-#pragma unroll
-            for (int j = 0; j < kBatchV; ++j) {
-                const int i4 = base + j * kT + tid;
-                v[j] = i4 < vec_n ? __ldcg(reinterpret_cast<const float4 *>(s) + i4)
-                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            }
+            if (base > 0)
+                load_batch(base);
 #pragma unroll
             for (int j = 0; j < kBatchV; ++j) {
                 const int i4 = base + j * kT + tid;
@@ -553,6 +571,7 @@ __device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned 
                             const unsigned slot = atomicAdd(&sm.cand_count, 1u);
                             cand_key[slot] = key[e];
                             cand_pos[slot] = pos0 + e;
+                            atomicAdd(&sm.hist2[(key[e] >> kShift2) & 0xffu], 1u);
                         }
                 }
             }
@@ -583,6 +602,7 @@ __device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned 
                         const unsigned slot = slot0 + __popc(m & ((1u << lane) - 1u));
                         cand_key[slot] = key;
                         cand_pos[slot] = i;
+                        atomicAdd(&sm.hist2[(key >> kShift2) & 0xffu], 1u);
                     }
                 }
             }
@@ -604,14 +624,17 @@ __device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned 
             __syncthreads();
         }
         if (use_bitmap) {
-            // write the set in position order by scanning the bitmap (no second row read)
+            // write the set in position order by scanning the bitmap (no second
+            // row read); the row's words are spread evenly over the threads
             const int words = (n + 31) / 32;
+            const int wpt = (words + kT - 1) / kT;  // <= kWordsPerThread
+            const int w0 = tid * wpt;
             unsigned w[kWordsPerThread];
             unsigned count = 0;
 #pragma unroll
             for (int j = 0; j < kWordsPerThread; ++j) {
-                const int wi = tid * kWordsPerThread + j;
-                w[j] = wi < words ? sm.bitmap[wi] : 0u;
+                const int wi = w0 + j;
+                w[j] = (j < wpt && wi < words) ? sm.bitmap[wi] : 0u;
                 count += __popc(w[j]);
             }
             unsigned total;
@@ -623,7 +646,7 @@ __device__ __noinline__ void topk_row(const TopkArgs &a, int g, int b, unsigned 
                     const int bit = __ffs(word) - 1;
                     word &= word - 1u;
                     if (slot < (unsigned)k)  // exactly k bits are set; the bound only guards memory
-                        out[slot] = (tid * kWordsPerThread + j) * 32 + bit;
+                        out[slot] = (w0 + j) * 32 + bit;
                     ++slot;
                 }
             }
@@ -813,8 +836,10 @@ topk_cluster_kernel(const TopkArgs a)
         for (int i = tid; i < kBins1; i += kT)
             sm.hist[i] = row_hist[i];
     }
-    if (tid == 0)
+    if (tid == 0) {
         sm.cand_count = 0u;
+        sm.short_count = 0u;
+    }
     __syncthreads();
     find_digit<kBins1>(sm, sm.hist, (unsigned)k);
     const uint32_t d1 = sm.res[0];
@@ -833,10 +858,13 @@ topk_cluster_kernel(const TopkArgs a)
 
     for (int w = tid; w < (len + 31) / 32; w += kT)
         sm.bitmap[w] = 0u;
+    for (int i = tid; i < 256; i += kT)
+        sm.hist2[i] = 0u;
     __syncthreads();
     const uint32_t prefix1 = d1 << (32 - kBits1);
     const uint32_t mask1 = ~0u << (32 - kBits1);
     const uint32_t top_of_bin = prefix1 | ~mask1;
+    constexpr int kShift2 = 32 - kBits1 - 8;  // second digit: key bits 20..13
     // whole float4 groups (lo is a multiple of 128, so the slice keeps the
     // row's 16-byte alignment): a warp covers 128 positions = 4 bitmap words
     const int vec_n = (((uintptr_t)s & 15u) == 0) ? len / 4 : 0;
@@ -876,6 +904,7 @@ topk_cluster_kernel(const TopkArgs a)
                         const unsigned slot = atomicAdd(&sm.cand_count, 1u);
                         cand_key[slot] = key[e];
                         cand_pos[slot] = lo + pos0 + e;
+                        atomicAdd(&sm.hist2[(key[e] >> kShift2) & 0xffu], 1u);
                     }
             }
         }
@@ -889,6 +918,7 @@ topk_cluster_kernel(const TopkArgs a)
             const unsigned slot = atomicAdd(&sm.cand_count, 1u);
             cand_key[slot] = key;
             cand_pos[slot] = lo + i;
+            atomicAdd(&sm.hist2[(key >> kShift2) & 0xffu], 1u);
         }
     }
     __syncthreads();
@@ -896,7 +926,14 @@ topk_cluster_kernel(const TopkArgs a)
     cluster.sync();  // every rank's pairs are complete
 
     if (rank == 0) {
-        // gather the other ranks' pairs behind this rank's own, then select
+        // gather the other ranks' pairs behind this rank's own, and add their
+        // second-digit counts to this rank's, then select
+        for (int i = tid; i < 256; i += kT) {
+            unsigned t = sm.hist2[i];
+            for (int rr = 1; rr < CS; ++rr)
+                t += *cluster.map_shared_rank(&sm.hist2[i], rr);
+            sm.hist2[i] = t;
+        }
         unsigned total = own;
         for (int rr = 1; rr < CS; ++rr) {
             const unsigned cnt = *cluster.map_shared_rank(&sm.cand_count, rr);
@@ -926,12 +963,14 @@ topk_cluster_kernel(const TopkArgs a)
     // positions kept by this slice, then their order within the slice
     constexpr int kWordsPerThread = C::kWordsPerThread;
     const int words = (len + 31) / 32;
+    const int wpt = (words + kT - 1) / kT;  // the slice's words spread evenly, <= kWordsPerThread
+    const int w0 = tid * wpt;
     unsigned w[kWordsPerThread];
     unsigned count = 0;
 #pragma unroll
     for (int j = 0; j < kWordsPerThread; ++j) {
-        const int wi = tid * kWordsPerThread + j;
-        w[j] = wi < words ? sm.bitmap[wi] : 0u;
+        const int wi = w0 + j;
+        w[j] = (j < wpt && wi < words) ? sm.bitmap[wi] : 0u;
         count += __popc(w[j]);
     }
     unsigned slice_total;
@@ -953,7 +992,7 @@ topk_cluster_kernel(const TopkArgs a)
             const int bit = __ffs(word) - 1;
             word &= word - 1u;
             if (slot < (unsigned)k)  // exactly k bits are set over all slices
-                out[slot] = lo + (tid * kWordsPerThread + j) * 32 + bit;
+                out[slot] = lo + (w0 + j) * 32 + bit;
             ++slot;
         }
     }
