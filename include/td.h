@@ -380,9 +380,12 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          tensor-core full (and full+select) / sparse kernel takes per round:
  *          8 (CTAs of 8 warps) or 16 (CTAs of 4 warps, both row groups of the
  *          MMA); 32 takes 16 per round with two rounds in flight per warp
- *          (the next round requested before this one's arithmetic); defaults
- *          16 for full layers; for sparse layers 32 when a CTA gathers at
- *          least 1024 rows, else 8; other values restore the default
+ *          (the next round requested before this one's arithmetic); 64
+ *          (sparse only) stages a CTA's rounds in a ring of shared-memory
+ *          buffers, two rounds in flight ahead of the one computed; defaults
+ *          16 for full layers; for sparse layers 64 when a CTA gathers at
+ *          least 1024 rows or a (batch row, KV head) is split over several
+ *          CTAs, else 8; other values restore the default
  *   "wait_limit_us": microseconds after which a staged full-layer CTA stops
  *          waiting for a bulk copy (default 1 s).  A CTA that gives up waits
  *          (at the default limit) for every copy it issued, then joins the

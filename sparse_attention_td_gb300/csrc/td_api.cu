@@ -48,8 +48,9 @@ struct Tuning {
                                  // whole waves of CTAs (stream-K), 0 one CTA per split
     int mma_full_tokens = 16;    // tensor-core full / full+select kernels: tokens per warp per round
     int mma_sparse_tokens = 0;   // tensor-core sparse kernels: tokens per warp per round (8, 16, or
-                                 // 32 = 16 with two rounds in flight); 0: 32 when a CTA's chunk
-                                 // holds >= kLongSparseChunk entries, else 8
+                                 // 32 = 16 with two rounds in flight, 64 = rounds staged in shared
+                                 // memory); 0: 64 when a CTA's chunk holds >= kLongSparseChunk
+                                 // entries or a pair has several splits, else 8
     int wait_limit_us = 0;       // staged full layers: microseconds a stage wait may take before it
                                  // gives up and the launch reports TD_FLAG_WAIT_TIMEOUT (0: 1 s)
     int wait_test = 0;           // 1: each staged full-layer CTA's first wait polls a barrier that
@@ -75,21 +76,26 @@ int prefetch_for(int G)
     return g_tuning.full_prefetch < 0 ? (mma_for(G) ? 1 : 0) : g_tuning.full_prefetch;
 }
 
-// Measured on GB300: two rounds in flight per warp (16-token kernel, 2 CTAs
-// per SM) take 4% off sparse layers whose CTAs gather 2048 rows (serving
-// batch, k = 4096), are even at 1024 and lose 9-10% on CTAs of ~250 rows,
-// where the 8-token kernel (also 2 CTAs per SM, so the same split plan) stays.
+// Measured on GB300 (graph steps): sparse layers staged through the
+// shared-memory ring (its first two rounds requested before the wait for the
+// previous kernel) beat the 8-token register kernel where a pair's rows are
+// split over several CTAs (32K: 765 -> 756 us, the prefetch overlaps the
+// split merge of the layer before) and where CTAs gather >= 1024 rows
+// (serving batch k = 1024: 1861 -> 1830 us; k = 4096: 4094 -> 3954 us, also
+// ahead of the 16-token kernel with two rounds in flight); on one-split
+// layers of 256-row CTAs (serving batch k = 256) they lose 0.4-3 us a layer.
 constexpr int kLongSparseChunk = 1024;
 
-// Tokens per warp per round of a tensor-core launch; chunk: index entries
-// per CTA of a sparse launch (its split plan is the same for 8 and 32).
-int mma_tokens_for(bool sparse, int chunk = 0)
+// Tokens per warp per round of a tensor-core launch (64: the sparse ring
+// kernel); chunk and nsplit: index entries per CTA and splits per (batch
+// row, KV head) of a sparse launch (the split plan is the same for 8 and 64).
+int mma_tokens_for(bool sparse, int chunk = 0, int nsplit = 1)
 {
     if (!sparse)
         return g_tuning.mma_full_tokens;
     if (g_tuning.mma_sparse_tokens > 0)
         return g_tuning.mma_sparse_tokens;
-    return chunk >= kLongSparseChunk ? 32 : 8;
+    return (chunk >= kLongSparseChunk || nsplit > 1) ? 64 : 8;
 }
 
 int device_sm_count();
@@ -548,7 +554,8 @@ td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
         a.tma_rows = (int)rows;
     }
     const cudaError_t le =
-        mma_for(c.G) ? td::launch_attention_mma(c.G, true, false, mma_tokens_for(true, a.chunk), a,
+        mma_for(c.G) ? td::launch_attention_mma(c.G, true, false,
+                                                mma_tokens_for(true, a.chunk, a.nsplit), a,
                                                 c.shape.batch, pdl, st)
                      : td::launch_attention(c.G, true, false, cluster, staged, a,
                                             c.shape.batch, pdl, st);
@@ -1014,7 +1021,9 @@ td_status td_set_tuning(const char *key, int32_t value)
             (value == 8 || value == 16 || value == 32) ? value : kDefaultTuning.mma_full_tokens;
     else if (!strcmp(key, "mma_sparse_tokens"))
         g_tuning.mma_sparse_tokens =
-            (value == 8 || value == 16 || value == 32) ? value : kDefaultTuning.mma_sparse_tokens;
+            (value == 8 || value == 16 || value == 32 || value == 64)
+                ? value
+                : kDefaultTuning.mma_sparse_tokens;
     else if (!strcmp(key, "wait_limit_us"))
         g_tuning.wait_limit_us = value > 0 ? value : kDefaultTuning.wait_limit_us;
     else if (!strcmp(key, "wait_test"))
@@ -1046,8 +1055,9 @@ const char *td_kernel_name(const td_shape *shape, int32_t top_k, int32_t sparse)
     if (mma_for(G)) {
         if (sp && g_tuning.sparse_stream_k > 0)
             return "attention_mma16_kernel (tensor cores, 16 tokens per warp, stream-K partition)";
-        const int t = mma_tokens_for(sp, chunk);
-        return t == 32   ? "attention_mma16_kernel (tensor cores, 16 tokens per warp, two rounds in flight)"
+        const int t = mma_tokens_for(sp, chunk, nsplit);
+        return t == 64   ? "attention_mma_ring_kernel (tensor cores, rounds staged in shared memory)"
+               : t == 32 ? "attention_mma16_kernel (tensor cores, 16 tokens per warp, two rounds in flight)"
                : t == 16 ? "attention_mma16_kernel (tensor cores, 16 tokens per warp)"
                          : "attention_mma_kernel (tensor cores, 8 tokens per warp)";
     }

@@ -6,20 +6,25 @@
 // query heads done by mma.sync m16n8k16 (bf16 inputs, fp32 accumulation):
 //   S[token][head] = K Q^T   (M = tokens, N = heads padded to 8, K = dims)
 //   O[dim][head]  += V^T P^T (M = dims,   N = heads,              K = tokens)
-// Two kernels, the same arithmetic, different tiling:
+// Three kernels, the same arithmetic, different tiling:
 //   * attention_mma_kernel: a warp takes 8 tokens per round (MMA rows 8..15
 //     of S and tokens 8..15 of the P V k-step stay zero), a CTA of 8 warps
-//     64 tokens; 2 CTAs per SM.  Default for sparse layers.
+//     64 tokens; 2 CTAs per SM.  Default for sparse layers of one short CTA
+//     per (batch row, KV head).
+//   * attention_mma_ring_kernel: the same 8-token rounds for sparse layers,
+//     gathered into a ring of shared-memory stages by cp.async and read back
+//     by ldmatrix, two rounds in flight ahead of the one computed.  Default
+//     for the other sparse layers.
 //   * attention_mma16_kernel: a warp takes 16 tokens per round (rows r and
 //     r + 8 of S are two tokens, the P V k-step takes all 16), a CTA of 4
 //     warps 64 tokens; half the MMAs and shuffles per token, 3 CTAs per SM.
 //     Default for full and full+select layers.
 // Measured on GB300: the 16-token kernel takes 2-6% off full and full+select
 // layers, but is slower on sparse layers whose CTAs are short and
-// latency-bound; there the 8-token kernel stays.  The splits of
-// either merge as in the CUDA-core kernels.
+// latency-bound.  The splits of each merge as in the CUDA-core kernels.
 //
-// Fragments come straight from global memory.  The dot product does not care
+// In the first and last kernels fragments come straight from global memory
+// (the ring kernel's layout is described with it).  The dot product does not care
 // in which order the 128 dims are summed, so k-step j of the S product maps
 // MMA column pairs {2c, 2c+1} / {2c+8, 2c+9} of lane quad position c to dims
 // 16j + 4c + {0,1} / {2,3}: a lane reads 8 bytes of its token's K row (and of
@@ -319,6 +324,304 @@ attention_mma_kernel(const AttnArgs a)
             if (sm_hist[i])
                 atomicAdd(&gh[i], sm_hist[i]);
     }
+    if (tid < G) {
+        const int h = tid;
+        float M = -CUDART_INF_F;
+        for (int w = 0; w < kAttnWarps; ++w)
+            M = fmaxf(M, sm_m[w][h]);
+        float L = 0.0f;
+        for (int w = 0; w < kAttnWarps; ++w) {
+            const float wt = safe_exp2_diff(sm_m[w][h], M);
+            sm_w[w][h] = wt;
+            L += sm_l[w][h] * wt;
+        }
+        sm_M[h] = M;
+        sm_L[h] = L;
+    }
+    __syncthreads();
+    const size_t out_row0 = (size_t)b * a.Hq + (size_t)g * G;
+    finish_splits<G>(a, sm_o, sm_w, sm_M, sm_L, &sm_last, bg, split, nsplit_b, out_row0);
+}
+
+// Sparse layers through a ring of shared-memory stages: a stage holds one
+// CTA round of gathered rows (64 K rows and their 64 V rows, 32 KB) copied by
+// cp.async, 16 bytes a thread and copy; kRingStages stages, so kRingStages - 1
+// rounds are in flight while one is computed, and the first of them are
+// requested before the wait for the previous kernel.  Padding and positions
+// past the split are zero-filled (their logits are masked; V must stay
+// finite).  The 16-byte chunks of each stored row are XOR-swizzled by the row
+// (chunk q of row t at q ^ (t & 7)), so the 8 row addresses of one ldmatrix
+// fall in 8 different bank groups.  Fragments take the standard m16n8k16
+// layout, straight from ldmatrix:
+//   S = K q^T: A = K of the warp's 8 tokens (rows 8..15 zero), k-step j =
+//     dims 16j .. 16j + 15; B = q^T, dims 16j + 2c, +1 and 16j + 8 + 2c, +1
+//     of head r (loaded once from global);
+//   O += V^T P^T: A = V^T by ldmatrix.trans, rows r / r + 8 of m-tile t =
+//     dims 16t + r / 16t + 8 + r, k = the warp's 8 tokens (8..15 zero);
+//     B = P^T as in attention_mma_kernel.
+// The warps' partial outputs reuse the ring once the last round is done.
+constexpr int kRingStages = 3;
+constexpr int kRingRowBytes = kHeadDim * 2;                          // 256
+constexpr int kRingStageBytes = 2 * kTokPerRound * kRingRowBytes;    // K block + V block
+constexpr int kRingSmemBytes = kRingStages * kRingStageBytes;        // 96 KB
+
+__device__ __forceinline__ uint32_t shared_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte global -> shared copy through L2 (cp.async.cg); zero-fills the
+// destination instead when !valid (src is then not read).
+__device__ __forceinline__ void cp_async16_or_zero(uint32_t dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit_group()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Four 8x8 bf16 matrices from shared memory; lanes 8m .. 8m + 7 give the row
+// addresses of matrix m, register m receives its fragment.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &d0, uint32_t &d1, uint32_t &d2,
+                                        uint32_t &d3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// The same, each matrix transposed.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &d0, uint32_t &d1,
+                                              uint32_t &d2, uint32_t &d3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+template <int G>
+__global__ void __launch_bounds__(kAttnThreads, 2)
+attention_mma_ring_kernel(const AttnArgs a)
+{
+    static_assert(G == 4 || G == 8, "heads of a group are the MMA's N = 8 columns");
+    static_assert(kAttnWarps * G * kHeadDim * 4 <= kRingSmemBytes, "sm_o fits in the ring");
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ float sm_m[kAttnWarps][G];
+    __shared__ float sm_l[kAttnWarps][G];
+    __shared__ float sm_w[kAttnWarps][G];
+    __shared__ float sm_M[G];
+    __shared__ float sm_L[G];
+    __shared__ int sm_rows[kMaxSparseChunk];
+    __shared__ int sm_last;
+    float(*sm_o)[G][kHeadDim] = reinterpret_cast<float(*)[G][kHeadDim]>(ring);
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = lane >> 2, c = lane & 3;  // MMA fragment row group / quad position
+
+    int n_b = a.seq_lens[b];
+    if (n_b < 0 || n_b > a.Nmax) {
+        if (tid == 0)
+            atomicOr(a.status, kFlagSeqLenOutOfRange);
+        n_b = n_b < 0 ? 0 : a.Nmax;
+    }
+    const int n_total = a.top_k;
+    const int nsplit_b = n_total > 0 ? (n_total + a.chunk - 1) / a.chunk : 1;
+    if (split >= nsplit_b)
+        return;
+    const int t0 = split * a.chunk;
+    const int t1 = min(t0 + a.chunk, n_total);
+    const size_t bg = (size_t)b * a.Hkv + g;
+    const uint16_t *kbase = a.k + bg * (size_t)a.Nmax * kHeadDim;
+    const uint16_t *vbase = a.v + bg * (size_t)a.Nmax * kHeadDim;
+
+    if (a.idx_dep)
+        pdl_wait();
+    const int32_t *ip = a.idx + bg * (size_t)a.top_k;
+    for (int j = tid; j < t1 - t0; j += kAttnThreads) {
+        int rr = ip[t0 + j];
+        if (rr < -1 || rr >= n_b) {
+            atomicOr(a.status, kFlagIndexOutOfRange);
+            rr = -1;
+        }
+        sm_rows[j] = rr;
+    }
+    __syncthreads();
+
+    // Stage `it` holds the rows of tokens t0 + 64 it ..; each warp copies the
+    // 8 rows it computes (stage rows 8 warp ..), one token per step: lanes
+    // 0-15 the K row's 16-byte chunks, lanes 16-31 the V row's.
+    const int n_it = (t1 - t0 + kTokPerRound - 1) / kTokPerRound;
+    const uint32_t ring_s = shared_addr(ring);
+    auto issue = [&](int it) {
+        const uint32_t st = ring_s + (uint32_t)((it % kRingStages) * kRingStageBytes);
+        const int tl = t0 + it * kTokPerRound + warp * 8 + (lane & 7);
+        const int pl = tl < t1 ? sm_rows[tl - t0] : -1;
+        const int q = lane & 15;
+        const uint32_t dst0 = st + (lane < 16 ? 0u : (uint32_t)(kRingStageBytes / 2)) +
+                              (uint32_t)(warp * 8 * kRingRowBytes);
+        const uint16_t *src0 = (lane < 16 ? kbase : vbase) + q * 8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int p = __shfl_sync(kFull, pl, j);
+            cp_async16_or_zero(dst0 + (uint32_t)(j * kRingRowBytes + ((q ^ j) << 4)),
+                               src0 + (size_t)(p >= 0 ? p : 0) * kHeadDim, p >= 0);
+        }
+    };
+    // the cache is never written by a kernel of the step
+    for (int st = 0; st < kRingStages - 1; ++st) {
+        if (st < n_it)
+            issue(st);
+        cp_async_commit_group();
+    }
+    pdl_wait();
+
+    // q^T fragments of head r (heads >= G are zero columns)
+    uint32_t qb0[8], qb1[8];
+    {
+        const uint16_t *qrow = a.q + ((size_t)b * a.Hq + (size_t)g * G + r) * kHeadDim;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            qb0[j] = r < G ? *reinterpret_cast<const uint32_t *>(qrow + 16 * j + 2 * c) : 0u;
+            qb1[j] = r < G ? *reinterpret_cast<const uint32_t *>(qrow + 16 * j + 8 + 2 * c) : 0u;
+        }
+    }
+
+    const float c2 = a.scale * kLog2e;
+    float m[2] = {-CUDART_INF_F, -CUDART_INF_F};  // heads 2c, 2c+1 (replicated over r)
+    float l[2] = {0.0f, 0.0f};
+    // m-tile t: o[t][0, 1] = O[dim 16t + r][heads 2c, 2c+1], o[t][2, 3] = dim 16t + 8 + r
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[i][j] = 0.0f;
+
+    const int lrow = warp * 8 + (lane & 7);  // stage row whose address this lane gives ldmatrix
+    const int lmat = lane >> 3;              // the matrix of the x4 it belongs to
+    for (int it = 0; it < n_it; ++it) {
+        if (it + kRingStages - 1 < n_it)
+            issue(it + kRingStages - 1);  // into the slice this warp finished last round
+        cp_async_commit_group();
+        cp_async_wait_group<kRingStages - 1>();  // this lane's copies of stage `it` landed
+        __syncwarp();                            // ... and the other lanes' of this warp
+        const uint32_t kst = ring_s + (uint32_t)((it % kRingStages) * kRingStageBytes);
+        const uint32_t vst = kst + kRingStageBytes / 2;
+        const uint32_t lrow_off = (uint32_t)(lrow * kRingRowBytes);
+        const int tw = t0 + it * kTokPerRound + warp * 8;  // this warp's 8 tokens
+
+        // S = K q^T: ldmatrix x4 jj gives k-steps 2jj and 2jj + 1 (dim chunks 4jj .. 4jj + 3)
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s_odd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int q = 4 * jj + lmat;
+            uint32_t k0, k1, k2, k3;
+            ldsm_x4(kst + lrow_off + (uint32_t)((q ^ (lrow & 7)) << 4), k0, k1, k2, k3);
+            mma_bf16(s, k0, 0u, k1, 0u, qb0[2 * jj], qb1[2 * jj]);
+            mma_bf16(s_odd, k2, 0u, k3, 0u, qb0[2 * jj + 1], qb1[2 * jj + 1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            s[e] += s_odd[e];
+        const bool ok = tw + r < t1 && sm_rows[tw + r - t0] >= 0;
+
+        // online softmax of heads 2c, 2c+1 over the warp's 8 tokens
+        float p[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool head = 2 * c + e < G;
+            const float x = (ok && head) ? s[e] * c2 : -CUDART_INF_F;
+            float mx = x;
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+            const float m_new = fmaxf(m[e], mx);
+            float alpha = 1.0f;
+            p[e] = 0.0f;
+            if (m_new != -CUDART_INF_F) {  // uniform over the 8 lanes of this head
+                alpha = safe_exp2_diff(m[e], m_new);
+                p[e] = (x == -CUDART_INF_F) ? 0.0f : exp2f(x - m_new);
+            }
+            float ps = p[e];
+            ps += __shfl_xor_sync(kFull, ps, 4);
+            ps += __shfl_xor_sync(kFull, ps, 8);
+            ps += __shfl_xor_sync(kFull, ps, 16);
+            if (m_new != -CUDART_INF_F) {
+                l[e] = l[e] * alpha + ps;
+                m[e] = m_new;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    o[i][e] *= alpha;
+                    o[i][e + 2] *= alpha;
+                }
+            }
+        }
+
+        // P^T fragment: P[token 2c][head r], P[token 2c+1][head r], held by
+        // lanes (row 2c / 2c+1, quad r / 2) in register r & 1
+        const int src0 = 8 * c + (r >> 1), src1 = 8 * c + 4 + (r >> 1);
+        const float a0p = __shfl_sync(kFull, p[0], src0), a1p = __shfl_sync(kFull, p[1], src0);
+        const float b0p = __shfl_sync(kFull, p[0], src1), b1p = __shfl_sync(kFull, p[1], src1);
+        float pt0 = (r & 1) ? a1p : a0p;
+        float pt1 = (r & 1) ? b1p : b0p;
+        uint32_t pb[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {  // p = p1 + p2 + p3 in bf16
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(pt0), h1 = __float2bfloat16_rn(pt1);
+            pb[k] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+            pt0 -= __bfloat162float(h0);
+            pt1 -= __bfloat162float(h1);
+        }
+        // O += V^T P^T: ldmatrix.trans x4 tt gives rows r and r + 8 of m-tiles
+        // 2tt and 2tt + 1 (dim chunks 4tt .. 4tt + 3)
+        uint32_t va[8], vb[8];
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+            const int q = 4 * tt + lmat;
+            ldsm_x4_trans(vst + lrow_off + (uint32_t)((q ^ (lrow & 7)) << 4), va[2 * tt],
+                          vb[2 * tt], va[2 * tt + 1], vb[2 * tt + 1]);
+        }
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                mma_bf16(o[i], va[i], vb[i], 0u, 0u, pb[k], 0u);
+        __syncwarp();  // every lane is done with this slice before it is refilled
+    }
+
+    pdl_launch_dependents();
+    __syncthreads();  // every warp is done with the ring, which sm_o reuses
+
+    // this warp's partial into shared memory
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int h = 2 * c + e;
+        if (h < G) {
+            if (r == 0) {
+                sm_m[warp][h] = m[e];
+                sm_l[warp][h] = l[e];
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                sm_o[warp][h][16 * t + r] = o[t][e];
+                sm_o[warp][h][16 * t + 8 + r] = o[t][e + 2];
+            }
+        }
+    }
+    __syncthreads();
     if (tid < G) {
         const int h = tid;
         float M = -CUDART_INF_F;
@@ -709,8 +1012,27 @@ int occupancy(Kern kern, int threads)
     return n > 0 ? n : 1;
 }
 
+// The ring kernel's shared-memory opt-in, once per device.
+template <int G>
+cudaError_t configure_ring()
+{
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64 && configured[dev])
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(attention_mma_ring_kernel<G>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64)
+        configured[dev] = true;
+    return e;
+}
+
 // tokens: 8 (attention_mma_kernel), 16 (attention_mma16_kernel, one round in
-// flight per warp) or 32 (attention_mma16_kernel, two rounds in flight).
+// flight per warp), 32 (attention_mma16_kernel, two rounds in flight) or, for
+// sparse layers, 64 (attention_mma_ring_kernel, rounds staged in shared memory).
 // a.sk_ctas > 0 (sparse, tokens 16 or 32): the stream-K partition over a 1D
 // grid of a.sk_ctas CTAs for a.sk_units (batch row, KV head) pairs (partials
 // with a stride of a.nsplit per pair).
@@ -734,6 +1056,24 @@ cudaError_t launch_mma_one(int tokens, const AttnArgs &a, int batch, bool pdl, c
                        : cudaLaunchKernelEx(&cfg, attention_mma16_kernel<G, true, false, false, true>, sk);
         }
     }
+    if constexpr (SPARSE) {
+        if (tokens == 64) {
+            const cudaError_t e = configure_ring<G>();
+            if (e != cudaSuccess)
+                return e;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)a.nsplit, (unsigned)a.Hkv, (unsigned)batch);
+            cfg.blockDim = dim3(kAttnThreads);
+            cfg.dynamicSmemBytes = kRingSmemBytes;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, attention_mma_ring_kernel<G>, a);
+        }
+    }
     if (tokens == 32)
         return launch_kernel(attention_mma16_kernel<G, SPARSE, SELECT, true>, kMma16Threads, a,
                              batch, pdl, st);
@@ -746,6 +1086,15 @@ cudaError_t launch_mma_one(int tokens, const AttnArgs &a, int batch, bool pdl, c
 template <int G, bool SPARSE, bool SELECT>
 int mma_occupancy_one(int tokens)
 {
+    if (SPARSE && tokens == 64) {
+        if (configure_ring<G>() != cudaSuccess)
+            return 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_mma_ring_kernel<G>,
+                                                          kAttnThreads, kRingSmemBytes) != cudaSuccess)
+            return 1;
+        return n > 0 ? n : 1;
+    }
     if (tokens == 32)
         return occupancy(attention_mma16_kernel<G, SPARSE, SELECT, true>, kMma16Threads);
     if (tokens == 16)

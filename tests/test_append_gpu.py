@@ -37,6 +37,7 @@ PATHS = {
     "mma8": {"mma": 1, "mma_full_tokens": 8, "full_prefetch": 2},
     "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},
     "mma32": {"mma": 1, "mma_full_tokens": 32, "mma_sparse_tokens": 32},
+    "ring": {"mma": 1, "mma_sparse_tokens": 64},
     "stream_k": {"mma": 1, "sparse_stream_k": 1},
 }
 TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch", "mma_full_tokens",

@@ -47,10 +47,12 @@ NON_DEFAULT_PATHS = {
     "prefetch2": {"mma": 1, "full_prefetch": 2},
     "mma8": {"mma_full_tokens": 8},
     "mma16": {"mma_sparse_tokens": 16},
+    "ring": {"mma_sparse_tokens": 64},
     "stream_k": {"sparse_stream_k": 1},
 }
 PATH_CASES = [(p, "llama3-8b-32k") for p in NON_DEFAULT_PATHS] + [("tma", "llama2-7b-100k"),
-                                                                   ("stream_k", "serving-b32")]
+                                                                   ("stream_k", "serving-b32"),
+                                                                   ("ring", "serving-b32")]
 
 
 @pytest.mark.parametrize("name,k,n_groups", CASES, ids=[f"{c[0]}-k{c[1]}" for c in CASES])

@@ -34,6 +34,7 @@ PATHS = {
     "mma8": {"mma": 1, "mma_full_tokens": 8, "full_prefetch": 2},
     "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},
     "mma32": {"mma": 1, "mma_full_tokens": 32, "mma_sparse_tokens": 32},
+    "ring": {"mma": 1, "mma_sparse_tokens": 64},
     "stream_k": {"mma": 1, "sparse_stream_k": 1},
 }
 TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch", "mma_full_tokens",
@@ -51,8 +52,10 @@ def staged(request):
     layers), 8 tokens per warp for every layer kind, and 16 for every layer
     kind, these two also prefetching two rounds ahead into L2 on full layers
     (the default is one round); 16 tokens per warp with two rounds in
-    flight per warp for every layer kind; and sparse layers under the
-    stream-K partition (a 1D grid sharing the layer's rounds evenly)."""
+    flight per warp for every layer kind; sparse layers staged through a
+    ring of shared-memory rounds read back by ldmatrix; and sparse layers
+    under the stream-K partition (a 1D grid sharing the layer's rounds
+    evenly)."""
     for key, value in PATHS[request.param].items():
         td.td_set_tuning(key, value)
     yield request.param
