@@ -276,6 +276,33 @@ td_status td_plan_launch(td_plan *plan, void *stream);
 void td_plan_destroy(td_plan *plan);
 
 /*
+ * td_plan_create_host: td_plan_create whose step also moves its inputs and
+ * results between host and device, for callers whose q rows are produced,
+ * and whose outputs are consumed, on the host.  The pages describe no such
+ * call; it is the plumbing around the step.  Every layer's q rows and
+ * outputs live in one buffer per side:
+ *   q_host    HOST, page-locked (cudaHostAlloc / cudaHostRegister), bf16
+ *             [num_layers][B][Hq][128]: copied to q in one copy at the start
+ *             of the step.
+ *   q         DEVICE bf16 [num_layers][B][Hq][128]: layer l reads q + l*B*Hq*128.
+ *   outs      DEVICE bf16 [num_layers][B][Hq][128]: layer l writes outs + l*B*Hq*128.
+ *   out_host  HOST, page-locked, bf16 [num_layers][B][Hq][128]: receives outs;
+ *             layers 0 .. L-2 in one copy on a second stream of the graph
+ *             while the last layer runs, the last layer's after it.
+ * Other arguments as in td_plan_create (outs_f32 stay on the device).
+ * Pageable host memory is rejected with TD_ERR_INVALID_ARG (nothing
+ * captured).  Each host range must lie in one page-locked allocation.  The
+ * buffers must stay allocated while the plan lives; the step's results are
+ * in out_host once the launch's stream has completed.
+ */
+td_status td_plan_create_host(td_plan **plan, const td_shape *shape, int32_t num_layers,
+                              const int32_t *modes, const void *q_host, void *q,
+                              const void *const *k_caches, const void *const *v_caches,
+                              const int32_t *seq_lens, int32_t top_k, int32_t *idx_buf,
+                              int32_t idx_valid, void *outs, float *const *outs_f32,
+                              void *out_host, void *ws, size_t ws_bytes);
+
+/*
  * KV append: the decode step's new token joins each layer's cache before
  * that layer attends (the growing KV cache of the decode phase, review §二).
  * seq_lens[b] already counts the new token, which sits at position

@@ -89,6 +89,9 @@ def lib():
     L.td_plan_create_append.restype = ctypes.c_int
     L.td_plan_create_append.argtypes = [ctypes.POINTER(vp), shp, i32, vp, vpp, vpp, vpp, vpp, vpp,
                                         vp, i32, vp, i32, vpp, vpp, vp, sz]
+    L.td_plan_create_host.restype = ctypes.c_int
+    L.td_plan_create_host.argtypes = [ctypes.POINTER(vp), shp, i32, vp, vp, vp, vpp, vpp, vp,
+                                      i32, vp, i32, vp, vpp, vp, vp, sz]
     L.td_index_overlap.restype = ctypes.c_int
     L.td_index_overlap.argtypes = [shp, vp, vp, i32, vp, vp]
     L.td_sparse_attn.restype = ctypes.c_int
@@ -368,16 +371,54 @@ def td_decode_step(shape: Shape, modes: Sequence[int], q, k_caches, v_caches, se
     _check(st, "td_decode_step")
 
 
+def _one_buffer(ts, name, n):
+    """Device pointer of per-layer tensors that are consecutive slices of one
+    buffer (layer l at the start + l * n values)."""
+    base = ts[0].data_ptr()
+    for l, t in enumerate(ts):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.numel() != n or \
+                t.data_ptr() != base + 2 * n * l:
+            raise ValueError(f"{name}: the layers must be consecutive slices of one bf16 buffer")
+    return base
+
+
+def _host_buffer(t, name, n):
+    if t is None or t.is_cuda or t.dtype != torch.bfloat16 or t.numel() != n or \
+            not t.is_contiguous():
+        raise ValueError(f"{name}: one contiguous bf16 host tensor of {n} values expected")
+    if not t.is_pinned():
+        raise ValueError(f"{name}: the host tensor must be page-locked (pin_memory())")
+    return t.data_ptr()
+
+
 class Plan:
-    """A decode step captured once into a CUDA graph (td_plan_create)."""
+    """A decode step captured once into a CUDA graph (td_plan_create).  With
+    q_host / out_host (page-locked host tensors of all layers' rows, [L][B][Hq][128])
+    the step also copies the q rows in and the outputs back
+    (td_plan_create_host); q and outs must then be slices of one device
+    buffer each."""
 
     def __init__(self, shape: Shape, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf, outs,
-                 outs_f32=None, ws: Workspace = None, idx_valid=False, k_new=None, v_new=None):
+                 outs_f32=None, ws: Workspace = None, idx_valid=False, k_new=None, v_new=None,
+                 q_host=None, out_host=None):
         self._args = _StepArgs(shape, modes, q, k_caches, v_caches, seq_lens, top_k, idx_buf,
                                outs, outs_f32, k_new, v_new)
-        self._keep = (q, k_caches, v_caches, seq_lens, idx_buf, outs, outs_f32, ws, k_new, v_new)
+        self._keep = (q, k_caches, v_caches, seq_lens, idx_buf, outs, outs_f32, ws, k_new, v_new,
+                      q_host, out_host)
         self._plan = ctypes.c_void_p(0)
         a = self._args
+        if q_host is not None or out_host is not None:
+            if a.append:
+                raise ValueError("host q/out and KV append are separate plans")
+            n = shape.batch * shape.num_q_heads * shape.head_dim
+            qh = _host_buffer(q_host, "q_host", a.L * n)
+            oh = _host_buffer(out_host, "out_host", a.L * n)
+            st = lib().td_plan_create_host(
+                ctypes.byref(self._plan), ctypes.byref(shape), a.L, a.modes, qh,
+                _one_buffer(q, "q", n), a.k, a.v, a.seq, a.top_k, a.idx, int(bool(idx_valid)),
+                _one_buffer(outs, "outs", n), a.outs_f32, oh, ws.ptr, ws.nbytes)
+            _check(st, "td_plan_create_host")
+            return
         if a.append:
             st = lib().td_plan_create_append(
                 ctypes.byref(self._plan), ctypes.byref(shape), a.L, a.modes, a.q, a.k, a.v,
