@@ -728,6 +728,16 @@ attention_mma16_kernel(const AttnArgs a)
         t0 = split * a.chunk;
         t1 = min(t0 + a.chunk, n_total);
     }
+    // rounds of this CTA: t0, t0 + step, ... below t1 (interleaved: every
+    // nsplit_b-th round of the pair, starting at round `split`)
+    int step = kTokPerRound;
+    if constexpr (!SPARSE && !SK && !DB) {
+        if (a.interleave) {
+            t0 = split * kTokPerRound;
+            t1 = n_b;
+            step = nsplit_b * kTokPerRound;
+        }
+    }
     const size_t bg = (size_t)b * a.Hkv + g;
     const uint16_t *kbase = a.k + bg * (size_t)a.Nmax * kHeadDim;
     const uint16_t *vbase = a.v + bg * (size_t)a.Nmax * kHeadDim;
@@ -788,7 +798,7 @@ attention_mma16_kernel(const AttnArgs a)
     // ahead of use
     const int pf = SPARSE ? 0 : a.prefetch;
     for (int d = 1; d <= pf; ++d)
-        prefetch(t0 + d * kTokPerRound);
+        prefetch(t0 + d * step);
     pdl_wait();
 
     // q of head r (heads >= G are zero columns): dims 16j + 4c .. +3.
@@ -933,9 +943,9 @@ attention_mma16_kernel(const AttnArgs a)
     } else {
         if (t0 < t1)
             round(t0, kq0, vv0);
-        for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
+        for (int base = t0 + step; base < t1; base += step) {
             if (pf > 0)
-                prefetch(base + pf * kTokPerRound);
+                prefetch(base + pf * step);
             load(base, kq0, vv0);
             round(base, kq0, vv0);
         }

@@ -50,6 +50,7 @@ NON_DEFAULT_PATHS = {
     "mma16": {"mma_sparse_tokens": 16},
     "ring": {"mma_sparse_tokens": 64},
     "sparse8": {"mma_sparse_tokens": 8},
+    "chunked": {"full_interleave": 0},
     "stream_k": {"sparse_stream_k": 1},
 }
 PATH_CASES = [(p, "llama3-8b-32k") for p in NON_DEFAULT_PATHS] + [("tma", "llama2-7b-100k"),
@@ -70,7 +71,7 @@ def test_full_size_step_on_non_default_kernel_paths(path, workload):
         _step_against_oracle(workload, None, 3)
     finally:
         for key in ("mma", "full_staged", "sparse_staged", "full_prefetch", "mma_full_tokens",
-                    "mma_sparse_tokens", "sparse_stream_k"):
+                    "mma_sparse_tokens", "sparse_stream_k", "full_interleave"):
             td.td_set_tuning(key, -1)
 
 

@@ -35,10 +35,11 @@ PATHS = {
     "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},
     "mma32": {"mma": 1, "mma_full_tokens": 32, "mma_sparse_tokens": 32},
     "ring": {"mma": 1, "mma_sparse_tokens": 64},
+    "chunked": {"mma": 1, "full_interleave": 0},
     "stream_k": {"mma": 1, "sparse_stream_k": 1},
 }
 TUNING_KEYS = ("full_staged", "sparse_staged", "mma", "full_prefetch", "mma_full_tokens",
-               "mma_sparse_tokens", "sparse_stream_k")
+               "mma_sparse_tokens", "sparse_stream_k", "full_interleave")
 
 
 @pytest.fixture(scope="module", autouse=True, params=list(PATHS))
