@@ -414,9 +414,10 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          least 1024 rows or a (batch row, KV head) is split over several
  *          CTAs, else 8; other values restore the default
  *   "full_interleave": 1 (default) the splits of a (batch row, KV head) of a
- *          tensor-core full layer (16 tokens per warp, one round in flight)
- *          take its 64-token rounds in turn; 0 one contiguous chunk each;
- *          negative restores the default
+ *          full layer take its 64-token rounds in turn (tensor cores with 16
+ *          tokens per warp and one round in flight; CUDA cores register-
+ *          streamed); 0 one contiguous chunk each; negative restores the
+ *          default
  *   "wait_limit_us": microseconds after which a staged full-layer CTA stops
  *          waiting for a bulk copy (default 1 s).  A CTA that gives up waits
  *          (at the default limit) for every copy it issued, then joins the

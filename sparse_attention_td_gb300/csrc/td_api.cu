@@ -52,9 +52,9 @@ struct Tuning {
                                  // 32 = 16 with two rounds in flight, 64 = rounds staged in shared
                                  // memory); 0: 64 when a CTA's chunk holds >= kLongSparseChunk
                                  // entries or a pair has several splits, else 8
-    int full_interleave = 1;     // tensor-core full layers (16 tokens per warp): 1 the splits of a
-                                 // (batch row, KV head) take its 64-token rounds in turn, 0 one
-                                 // contiguous chunk each
+    int full_interleave = 1;     // full layers (tensor cores with 16 tokens per warp, or CUDA cores
+                                 // register-streamed): 1 the splits of a (batch row, KV head)
+                                 // take its 64-token rounds in turn, 0 one contiguous chunk each
     int wait_limit_us = 0;       // staged full layers: microseconds a stage wait may take before it
                                  // gives up and the launch reports TD_FLAG_WAIT_TIMEOUT (0: 1 s)
     int wait_test = 0;           // 1: each staged full-layer CTA's first wait polls a barrier that
@@ -450,9 +450,10 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
     a.hist = select ? (unsigned *)(c.wsb + c.ws.hist) : nullptr;
     a.prefetch = prefetch_for(c.G);
     // Measured on GB300 (graph steps): interleaved rounds keep a pair's CTAs
-    // reading neighbouring rows at any moment; serving batch 1833 -> 1808 us,
-    // 32K 753 -> 752 us (a read-only probe: grid-stride 6.9 TB/s against
-    // 5.8 TB/s for one contiguous chunk per CTA at 4 CTAs per SM).
+    // reading neighbouring rows at any moment; serving batch 1830 -> 1813 us
+    // (tensor cores), 100K 1423 -> 1410 us and 10K 285 -> 283 us (CUDA cores,
+    // register-streamed), 32K even (a read-only probe: grid-stride 6.9 TB/s
+    // against 5.8 TB/s for one contiguous chunk per CTA at 4 CTAs per SM).
     a.interleave = g_tuning.full_interleave;
     plan_splits(c.shape, c.shape.max_seq_len, false, select, a.nsplit, a.chunk);
     const bool cluster = g_tuning.cluster && a.nsplit > 1 && a.nsplit <= td::kPortableClusterSplits;

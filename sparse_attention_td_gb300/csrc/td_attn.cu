@@ -205,8 +205,18 @@ attention_kernel(const __grid_constant__ AttnArgs a)
     const bool idle = split >= nsplit_b;
     if (idle && !CLUSTER)
         return;
-    const int t0 = idle ? 0 : split * a.chunk;
-    const int t1 = idle ? 0 : min(t0 + a.chunk, n_total);
+    int t0 = idle ? 0 : split * a.chunk;
+    int t1 = idle ? 0 : min(t0 + a.chunk, n_total);
+    // register-streamed full layers, interleaved: this CTA takes every
+    // nsplit_b-th 64-token round of the pair, starting at round `split`
+    int step = kTokPerRound;
+    if constexpr (!SPARSE && !STAGED && !CLUSTER) {
+        if (a.interleave && !idle) {
+            t0 = split * kTokPerRound;
+            t1 = n_total;
+            step = nsplit_b * kTokPerRound;
+        }
+    }
     const size_t bg = (size_t)b * a.Hkv + g;
     const uint16_t *kbase = a.k + bg * (size_t)a.Nmax * kHeadDim + c * 8;
     const uint16_t *vbase = a.v + bg * (size_t)a.Nmax * kHeadDim + c * 8;
@@ -347,7 +357,7 @@ attention_kernel(const __grid_constant__ AttnArgs a)
     auto row_at = [&](int t) { return t < t1 ? t : -1; };
     const int pf = (STAGED || SPARSE) ? 0 : a.prefetch;
     for (int d = 1; d <= pf; ++d)
-        prefetch_round_l2(krows, vrows, t0 + d * kTokPerRound + warp * 8, lane, row_at);
+        prefetch_round_l2(krows, vrows, t0 + d * step + warp * 8, lane, row_at);
     pdl_wait();
 
     // This lane's 8 dims of the group's G queries, as 4 dim pairs.
@@ -564,11 +574,11 @@ attention_kernel(const __grid_constant__ AttnArgs a)
     } else {
         if (t0 < t1)
             round(t0, kr0, vr0, ok0);
-        for (int base = t0 + kTokPerRound; base < t1; base += kTokPerRound) {
+        for (int base = t0 + step; base < t1; base += step) {
             uint4 kr[U], vr[U];
             bool ok[U];
             if (pf > 0)
-                prefetch_round_l2(krows, vrows, base + pf * kTokPerRound + warp * 8, lane, row_at);
+                prefetch_round_l2(krows, vrows, base + pf * step + warp * 8, lane, row_at);
             load_round(base, kr, vr, ok);
             round(base, kr, vr, ok);
         }

@@ -56,8 +56,9 @@ struct AttnArgs {
     int chunk;               // tokens (full) or index entries (sparse) per split
     int nsplit;              // gridDim.x
     int prefetch;            // full layers: rounds ahead whose rows each warp prefetches into L2 (0: none)
-    int interleave;          // full layers (tensor cores, 16 tokens per warp): the splits of a (batch
-                             // row, KV head) take its 64-token rounds in turn instead of one chunk each
+    int interleave;          // full layers (tensor cores with 16 tokens per warp, CUDA cores
+                             // register-streamed): the splits of a (batch row, KV head) take its
+                             // 64-token rounds in turn instead of one chunk each
     int wait_limit_us;       // staged full layers: microseconds before a stage wait gives up (0: 1 s)
     int wait_test;           // staged full layers: each CTA's first wait polls a barrier nothing
                              // arrives on (tests of the failure report); 0 in normal use
