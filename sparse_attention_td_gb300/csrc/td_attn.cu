@@ -192,19 +192,19 @@ attention_kernel(const __grid_constant__ AttnArgs a)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int half = lane >> 4, c = lane & 15;
 
-    int n_b = a.seq_lens[b];
-    if (n_b < 0 || n_b > a.Nmax) {
-        if (tid == 0)
-            atomicOr(a.status, kFlagSeqLenOutOfRange);
-        n_b = n_b < 0 ? 0 : a.Nmax;
-    }
+    // (the length check reports once the index entries are requested)
+    const int n_raw = a.seq_lens[b];
+    const int n_b = n_raw < 0 ? 0 : (n_raw > a.Nmax ? a.Nmax : n_raw);
     const int n_total = SPARSE ? a.top_k : n_b;
     const int nsplit_b = n_total > 0 ? (n_total + a.chunk - 1) / a.chunk : 1;
     // A split past this row's work returns at once -- except in a cluster,
     // where it takes part in the merge with an empty range.
     const bool idle = split >= nsplit_b;
-    if (idle && !CLUSTER)
+    if (idle && !CLUSTER) {
+        if (tid == 0 && n_raw != n_b)
+            atomicOr(a.status, kFlagSeqLenOutOfRange);
         return;
+    }
     int t0 = idle ? 0 : split * a.chunk;
     int t1 = idle ? 0 : min(t0 + a.chunk, n_total);
     // register-streamed full layers, interleaved: this CTA takes every
@@ -234,17 +234,12 @@ attention_kernel(const __grid_constant__ AttnArgs a)
         // Stage this split's persisted positions once (every round reads
         // them from shared memory); -1 is padding, anything else outside
         // [0, n_b) is reported and skipped.
-        const int32_t *ip = a.idx + bg * (size_t)a.top_k;
-        for (int j = tid; j < t1 - t0; j += kAttnThreads) {
-            int r = ip[t0 + j];
-            if (r < -1 || r >= n_b) {
-                atomicOr(a.status, kFlagIndexOutOfRange);
-                r = -1;
-            }
-            sm_rows[j] = r;
-        }
+        stage_index_rows<kAttnThreads>(a.idx + bg * (size_t)a.top_k, t0, t1 - t0, n_b, a.status,
+                                       sm_rows, tid);
         __syncthreads();
     }
+    if (tid == 0 && n_raw != n_b)
+        atomicOr(a.status, kFlagSeqLenOutOfRange);
 
     // This half-warp's U tokens of the round starting at `base`: K and V rows
     // requested into registers (zero for tokens past the split or padding).

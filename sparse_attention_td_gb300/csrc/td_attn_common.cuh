@@ -60,6 +60,37 @@ __device__ __forceinline__ void prefetch_round_l2(const uint16_t *kbase, const u
     }
 }
 
+// Stages a sparse CTA's index entries ip[t0 + j], j < count <= kMaxSparseChunk,
+// into sm_rows[j]: -1 stays padding, anything else outside [0, n_b) is
+// reported and skipped.  Every entry is requested before any is checked (the
+// checks can report, so loads issued after them would wait for the previous
+// checks), so the loads overlap one another and the caller's load of n_b.
+// All NT threads call it; sm_rows is complete after the caller's barrier.
+template <int NT>
+__device__ __forceinline__ void stage_index_rows(const int32_t *ip, int t0, int count, int n_b,
+                                                 uint32_t *status, int *sm_rows, int tid)
+{
+    constexpr int kPer = (kMaxSparseChunk + NT - 1) / NT;
+    int rv[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int j = tid + u * NT;
+        rv[u] = j < count ? __ldcg(ip + t0 + j) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int j = tid + u * NT;
+        if (j < count) {
+            int rr = rv[u];
+            if (rr < -1 || rr >= n_b) {
+                atomicOr(status, kFlagIndexOutOfRange);
+                rr = -1;
+            }
+            sm_rows[j] = rr;
+        }
+    }
+}
+
 __device__ __forceinline__ void pdl_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");

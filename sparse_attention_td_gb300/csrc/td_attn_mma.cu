@@ -431,12 +431,9 @@ attention_mma_ring_kernel(const AttnArgs a)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = lane >> 2, c = lane & 3;  // MMA fragment row group / quad position
 
-    int n_b = a.seq_lens[b];
-    if (n_b < 0 || n_b > a.Nmax) {
-        if (tid == 0)
-            atomicOr(a.status, kFlagSeqLenOutOfRange);
-        n_b = n_b < 0 ? 0 : a.Nmax;
-    }
+    // the length check reports after the index entries are requested
+    const int n_raw = a.seq_lens[b];
+    const int n_b = n_raw < 0 ? 0 : (n_raw > a.Nmax ? a.Nmax : n_raw);
     const int n_total = a.top_k;
     const int nsplit_b = n_total > 0 ? (n_total + a.chunk - 1) / a.chunk : 1;
     if (split >= nsplit_b)
@@ -449,15 +446,10 @@ attention_mma_ring_kernel(const AttnArgs a)
 
     if (a.idx_dep)
         pdl_wait();
-    const int32_t *ip = a.idx + bg * (size_t)a.top_k;
-    for (int j = tid; j < t1 - t0; j += kAttnThreads) {
-        int rr = ip[t0 + j];
-        if (rr < -1 || rr >= n_b) {
-            atomicOr(a.status, kFlagIndexOutOfRange);
-            rr = -1;
-        }
-        sm_rows[j] = rr;
-    }
+    stage_index_rows<kAttnThreads>(a.idx + bg * (size_t)a.top_k, t0, t1 - t0, n_b, a.status,
+                                   sm_rows, tid);
+    if (tid == 0 && n_raw != n_b)
+        atomicOr(a.status, kFlagSeqLenOutOfRange);
     __syncthreads();
 
     // Stage `it` holds the rows of tokens t0 + 64 it ..; each warp copies the
