@@ -345,9 +345,11 @@ attention_mma_kernel(const AttnArgs a)
 
 // Sparse layers through a ring of shared-memory stages: a stage holds one
 // CTA round of gathered rows (64 K rows and their 64 V rows, 32 KB) copied by
-// cp.async, 16 bytes a thread and copy; kRingStages stages, so kRingStages - 1
-// rounds are in flight while one is computed, and the first of them are
-// requested before the wait for the previous kernel.  Padding and positions
+// cp.async, 16 bytes a lane and copy; each warp gathers the 8 rows it
+// computes, so warps wait only for their own copies (no block barrier in the
+// loop).  kRingStages stages, so kRingStages - 1 rounds are in flight while
+// one is computed, and the first of them are requested before the wait for
+// the previous kernel.  Padding and positions
 // past the split are zero-filled (their logits are masked; V must stay
 // finite).  The 16-byte chunks of each stored row are XOR-swizzled by the row
 // (chunk q of row t at q ^ (t & 7)), so the 8 row addresses of one ldmatrix
