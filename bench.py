@@ -305,7 +305,8 @@ def measured_traffic(workload: str, kernel: str):
 def consecutive_overlap(td, torch, wl, shape, q, K, V, seq, ws, device):
     """Mean fraction of layer l's top-k set that layer l+1 also selects
     (layers 2..L-1, every (batch row, KV head)), from td_full_attn_select sets
-    and td_index_overlap counts."""
+    and td_index_overlap counts; also the Jaccard index of the two sets (both
+    of size m = min(k, N_b), sharing c positions: c / (2m - c))."""
     if wl.layers < 4:
         return None
     sets = []
@@ -317,12 +318,14 @@ def consecutive_overlap(td, torch, wl, shape, q, K, V, seq, ws, device):
         sets.append(s)
     counts = torch.empty((wl.batch, wl.kv_heads), dtype=torch.int32, device=device)
     size = torch.clamp(seq.to(torch.float32), max=float(wl.top_k)).view(-1, 1)
-    rates = []
+    rates, jacc = [], []
     for a, b in zip(sets[:-1], sets[1:]):
         td.td_index_overlap(shape, a, b, wl.top_k, counts)
-        rates.append((counts.to(torch.float32) / size).mean().item())
+        c = counts.to(torch.float32)
+        rates.append((c / size).mean().item())
+        jacc.append((c / (2 * size - c)).mean().item())
     return {"mean": round(float(np.mean(rates)), 4), "min": round(float(np.min(rates)), 4),
-            "layers": f"2..{wl.layers - 1}"}
+            "jaccard_mean": round(float(np.mean(jacc)), 4), "layers": f"2..{wl.layers - 1}"}
 
 
 def coverage_layer(td, torch, wl, shape, q, K, V, seq, ws, device, flush_l2, stream,
