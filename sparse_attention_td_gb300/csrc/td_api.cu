@@ -55,6 +55,15 @@ struct Tuning {
     int full_interleave = 1;     // full layers (tensor cores with 16 tokens per warp, or CUDA cores
                                  // register-streamed): 1 the splits of a (batch row, KV head)
                                  // take its 64-token rounds in turn, 0 one contiguous chunk each
+    // Rounds before the end of its last round at which a CTA of the ring,
+    // register-streamed or 16-token full kernel lets the next kernel launch
+    // (always after its own wait for the previous kernel, so at most one more
+    // grid is launched ahead); 0: after the last round.  Measured on GB300
+    // (graph steps), 0 / 1 / 2 / 3 / 4 / 6: serving k=1024 1804 / 1793 /
+    // 1784 / 1770 / 1767 / 1781 us, 32K 755 / 747 / 747 / 745 / 744 / 745 us,
+    // 100K 1419 / 1414 / 1415 / 1414 / 1412 / 1414 us, serving k=4096
+    // 3844 / 3841 / 3826 / 3813 / - / 3808 us, 10K even.
+    int early_trigger = 4;
     int wait_limit_us = 0;       // staged full layers: microseconds a stage wait may take before it
                                  // gives up and the launch reports TD_FLAG_WAIT_TIMEOUT (0: 1 s)
     int wait_test = 0;           // 1: each staged full-layer CTA's first wait polls a barrier that
@@ -397,6 +406,7 @@ td::AttnArgs base_args(const Ctx &c, const void *q, const void *k, const void *v
                        const int32_t *seq_lens, void *out, float *out_f32)
 {
     td::AttnArgs a{};
+    a.early_trigger = g_tuning.early_trigger;
     a.q = (const uint16_t *)q;
     a.k = (const uint16_t *)k;
     a.v = (const uint16_t *)v;
@@ -1152,6 +1162,8 @@ td_status td_set_tuning(const char *key, int32_t value)
                 : kDefaultTuning.mma_sparse_tokens;
     else if (!strcmp(key, "full_interleave"))
         g_tuning.full_interleave = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.full_interleave);
+    else if (!strcmp(key, "early_trigger"))
+        g_tuning.early_trigger = (value >= 0 && value <= 64) ? value : kDefaultTuning.early_trigger;
     else if (!strcmp(key, "wait_limit_us"))
         g_tuning.wait_limit_us = value > 0 ? value : kDefaultTuning.wait_limit_us;
     else if (!strcmp(key, "wait_test"))

@@ -567,11 +567,20 @@ attention_kernel(const __grid_constant__ AttnArgs a)
             }
         }
     } else {
+        // rounds of this CTA: t0, t0 + step, ...; with early_trigger the next
+        // kernel may launch from the start of round n_rounds - early_trigger
+        const int n_rounds = t1 > t0 ? (t1 - t0 + step - 1) / step : 0;
+        const int trig = a.early_trigger > 0 ? max(n_rounds - a.early_trigger, 0) : -1;
+        if (trig == 0)
+            pdl_launch_dependents();
         if (t0 < t1)
             round(t0, kr0, vr0, ok0);
-        for (int base = t0 + step; base < t1; base += step) {
+        int ri = 1;
+        for (int base = t0 + step; base < t1; base += step, ++ri) {
             uint4 kr[U], vr[U];
             bool ok[U];
+            if (ri == trig)
+                pdl_launch_dependents();
             if (pf > 0)
                 prefetch_round_l2(krows, vrows, base + pf * step + warp * 8, lane, row_at);
             load_round(base, kr, vr, ok);

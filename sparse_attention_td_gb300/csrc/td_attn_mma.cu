@@ -507,6 +507,8 @@ attention_mma_ring_kernel(const AttnArgs a)
     const int lrow = warp * 8 + (lane & 7);  // stage row whose address this lane gives ldmatrix
     const int lmat = lane >> 3;              // the matrix of the x4 it belongs to
     for (int it = 0; it < n_it; ++it) {
+        if (a.early_trigger > 0 && it == max(n_it - a.early_trigger, 0))
+            pdl_launch_dependents();
         if (it + kRingStages - 1 < n_it)
             issue(it + kRingStages - 1);  // into the slice this warp finished last round
         cp_async_commit_group();
@@ -935,9 +937,18 @@ attention_mma16_kernel(const AttnArgs a)
             }
         }
     } else {
+        // with early_trigger the next kernel may launch from the start of
+        // round n_rounds - early_trigger of this CTA
+        const int n_rounds = t1 > t0 ? (t1 - t0 + step - 1) / step : 0;
+        const int trig = (!SK && a.early_trigger > 0) ? max(n_rounds - a.early_trigger, 0) : -1;
+        if (trig == 0)
+            pdl_launch_dependents();
         if (t0 < t1)
             round(t0, kq0, vv0);
-        for (int base = t0 + step; base < t1; base += step) {
+        int ri = 1;
+        for (int base = t0 + step; base < t1; base += step, ++ri) {
+            if (ri == trig)
+                pdl_launch_dependents();
             if (pf > 0)
                 prefetch(base + pf * step);
             load(base, kq0, vv0);
