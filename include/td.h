@@ -414,7 +414,8 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          least 1024 rows or a (batch row, KV head) is split over several
  *          CTAs, else 8; other values restore the default
  *   "early_trigger": rounds before the end of its last round at which a
- *          CTA (ring, register-streamed and 16-token full kernels) lets the
+ *          CTA (ring, register-streamed, cp.async-staged sparse and 16-token
+ *          full kernels) lets the
  *          next kernel of the call launch; always after the CTA's own wait
  *          for the previous kernel (default 4; 0: after the last round;
  *          negative restores the default)

@@ -56,13 +56,15 @@ struct Tuning {
                                  // register-streamed): 1 the splits of a (batch row, KV head)
                                  // take its 64-token rounds in turn, 0 one contiguous chunk each
     // Rounds before the end of its last round at which a CTA of the ring,
-    // register-streamed or 16-token full kernel lets the next kernel launch
+    // register-streamed, cp.async-staged sparse or 16-token full kernel lets
+    // the next kernel launch
     // (always after its own wait for the previous kernel, so at most one more
     // grid is launched ahead); 0: after the last round.  Measured on GB300
     // (graph steps), 0 / 1 / 2 / 3 / 4 / 6: serving k=1024 1804 / 1793 /
     // 1784 / 1770 / 1767 / 1781 us, 32K 755 / 747 / 747 / 745 / 744 / 745 us,
     // 100K 1419 / 1414 / 1415 / 1414 / 1412 / 1414 us, serving k=4096
-    // 3844 / 3841 / 3826 / 3813 / - / 3808 us, 10K even.
+    // 3844 / 3841 / 3826 / 3813 / - / 3808 us, 10K 282.5 -> 280.4 us (4, with
+    // the cp.async-staged sparse layers).
     int early_trigger = 4;
     int wait_limit_us = 0;       // staged full layers: microseconds a stage wait may take before it
                                  // gives up and the launch reports TD_FLAG_WAIT_TIMEOUT (0: 1 s)

@@ -485,7 +485,10 @@ attention_kernel(const __grid_constant__ AttnArgs a)
     };
     if constexpr (STAGED == 1 && SPARSE) {
         const int slot0 = (warp * 2 + half) * U;
+        const int trig = a.early_trigger > 0 ? max(n_it - a.early_trigger, 0) : -1;
         for (int it = 0; it < n_it; ++it) {
+            if (it == trig)
+                pdl_launch_dependents();
             cp_async_wait<S - 1>();  // this thread's copies of stage `it` have landed
             const unsigned char *kst = sm_stage + (it % S) * kStageBytes;
             const unsigned char *vst = kst + kStageBytes / 2;

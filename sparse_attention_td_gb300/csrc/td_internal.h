@@ -57,8 +57,9 @@ struct AttnArgs {
     int nsplit;              // gridDim.x
     int prefetch;            // full layers: rounds ahead whose rows each warp prefetches into L2 (0: none)
     int early_trigger;       // >0: a CTA lets the next kernel launch at the start of its round
-                             // n_rounds - early_trigger (ring, register-streamed and 16-token full
-                             // kernels; after its wait for the previous kernel); 0: after the loop
+                             // n_rounds - early_trigger (ring, register-streamed, cp.async-staged
+                             // sparse and 16-token full kernels; after its wait for the previous
+                             // kernel); 0: after the loop
     int interleave;          // full layers (tensor cores with 16 tokens per warp, CUDA cores
                              // register-streamed): the splits of a (batch row, KV head) take its
                              // 64-token rounds in turn instead of one chunk each
