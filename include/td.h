@@ -361,6 +361,11 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          register-streamed sparse kernels that fit 4 or more per SM are
  *          planned one below it, leaving room for the next layer's CTAs)
  *   "full_waves", "sparse_waves": target waves of CTAs per launch
+ *   "sparse_splits": 1..256 splits per (batch, KV head) of sparse launches
+ *          (then kept within "max_splits", at most one per 64 entries, and
+ *          at least one per 2048 entries, the most a sparse CTA stages);
+ *          other values restore the default (from the CTAs per SM and the
+ *          waves)
  *   "max_splits": upper bound on splits per (batch, KV head)
  *   "cluster": 1 merges a (batch, KV head)'s splits (when 2..8) through a
  *              thread-block cluster; 0 (default) through global partials

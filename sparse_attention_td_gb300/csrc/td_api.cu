@@ -29,6 +29,8 @@ struct Tuning {
     int sparse_ctas_per_sm = 0;
     int full_waves = 0;          // 0 = auto (see plan_splits)
     int sparse_waves = 1;
+    int sparse_splits = 0;       // splits per (batch row, KV head) of sparse launches (0: from the
+                                 // CTAs per SM and waves above)
     int max_splits = td::kMaxSplits;
     int cluster = 0;             // 1: merge up to kPortableClusterSplits splits through a cluster
     int topk_threads = 0;        // 0 = 1024 threads per row, or 512
@@ -337,14 +339,17 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
     const int G = s.num_q_heads / s.num_kv_heads;
     const long units = (long)s.batch * s.num_kv_heads;
     int per_sm = sparse ? g_tuning.sparse_ctas_per_sm : g_tuning.full_ctas_per_sm;
+    int resident = per_sm;  // CTAs of the launched kernel that fit one SM
     if (per_sm <= 0) {
         const int staged = mma_for(G) ? 0 : staged_for(s, sparse, n_total);
         per_sm = mma_for(G) ? td::attention_mma_ctas_per_sm(G, sparse, select, mma_tokens_for(sparse))
                             : td::attention_ctas_per_sm(G, sparse, select, staged);
+        resident = per_sm;
         // Measured on GB300 (graph step): register-streamed sparse layers
         // planned one CTA per SM below the 4+ that fit leave a slot for the
         // next layer's CTAs to start early (100K MHA step 1438 -> 1426 us);
-        // at 2 per SM the launch loses half its warps and is slower.
+        // at 2 per SM the launch loses half its warps and is slower.  (One-wave
+        // sparse plans now take the whole-round rule below instead.)
         if (sparse && !mma_for(G) && staged == 0 && per_sm >= 4)
             per_sm -= 1;
     }
@@ -359,10 +364,31 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
         waves = units * 2 <= slots ? 1 : (mma_for(G) && !sparse ? 4 : 3);
     const long target = slots * waves;
     const int cap = split_cap(units, n_total, sparse);
+    const long len = n_total > 0 ? n_total : 1;
+    if (sparse && waves == 1 && g_tuning.sparse_splits <= 0) {
+        // One wave of sparse CTAs, each of whole 64-entry rounds: the fewest
+        // rounds a CTA can take within one wave at the kernel's occupancy,
+        // then the fewest splits that still take no more.  Measured on GB300
+        // (graph steps): 100K (MHA, k = 4096) 16 splits of 4 rounds 1398.5 us
+        // against 14 of 4.75 (the rule before) 1408.3 us, 19 of 3.4 1423.2 us
+        // and 13 of 5 1410.8 us; 32K (k = 2048) 8 splits of 4 rounds 738.5 us
+        // against 9 of 3.6 745.0 us; 4 to 6 splits and 10 or more (a second
+        // wave) slower at both.
+        long most = (long)device_sm_count() * resident / units;
+        if (most > cap) most = cap;
+        if (most < 1) most = 1;
+        long ch = ceil_div(ceil_div(len, most), td::kTokPerRound) * td::kTokPerRound;
+        if (ch > td::kMaxSparseChunk)
+            ch = td::kMaxSparseChunk;
+        nsplit = (int)ceil_div(len, ch);
+        chunk = (int)ch;
+        return;
+    }
     long want = target / units;  // whole waves: never spill a few CTAs into an extra wave
+    if (sparse && g_tuning.sparse_splits > 0)
+        want = g_tuning.sparse_splits;
     if (want < 1) want = 1;
     if (want > cap) want = cap;
-    const long len = n_total > 0 ? n_total : 1;
     long ch = ceil_div(ceil_div(len, want), td::kChunkGranule) * td::kChunkGranule;
     if (sparse && ch > td::kMaxSparseChunk)
         ch = td::kMaxSparseChunk;
@@ -1136,6 +1162,9 @@ td_status td_set_tuning(const char *key, int32_t value)
         g_tuning.full_waves = value > 0 ? value : kDefaultTuning.full_waves;
     else if (!strcmp(key, "sparse_waves"))
         g_tuning.sparse_waves = value > 0 ? value : kDefaultTuning.sparse_waves;
+    else if (!strcmp(key, "sparse_splits"))
+        g_tuning.sparse_splits = (value > 0 && value <= td::kMaxSplits) ? value
+                                                                       : kDefaultTuning.sparse_splits;
     else if (!strcmp(key, "cluster"))
         g_tuning.cluster = value > 0 ? 1 : 0;
     else if (!strcmp(key, "full_staged"))

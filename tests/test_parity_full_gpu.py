@@ -52,10 +52,14 @@ NON_DEFAULT_PATHS = {
     "sparse8": {"mma_sparse_tokens": 8},
     "chunked": {"full_interleave": 0},
     "stream_k": {"sparse_stream_k": 1},
+    # sparse CTAs ending in a part-filled 64-entry round (9 splits: 240
+    # entries a CTA at 32K, 464 at 100K); the default takes whole rounds
+    "splits9": {"sparse_splits": 9},
 }
 PATH_CASES = [(p, "llama3-8b-32k") for p in NON_DEFAULT_PATHS] + [("tma", "llama2-7b-100k"),
                                                                    ("stream_k", "serving-b32"),
-                                                                   ("sparse8", "serving-b32")]
+                                                                   ("sparse8", "serving-b32"),
+                                                                   ("splits9", "llama2-7b-100k")]
 
 
 @pytest.mark.parametrize("name,k,n_groups", CASES, ids=[f"{c[0]}-k{c[1]}" for c in CASES])
@@ -71,7 +75,7 @@ def test_full_size_step_on_non_default_kernel_paths(path, workload):
         _step_against_oracle(workload, None, 3)
     finally:
         for key in ("mma", "full_staged", "sparse_staged", "full_prefetch", "mma_full_tokens",
-                    "mma_sparse_tokens", "sparse_stream_k", "full_interleave"):
+                    "mma_sparse_tokens", "sparse_stream_k", "full_interleave", "sparse_splits"):
             td.td_set_tuning(key, -1)
 
 
