@@ -652,7 +652,12 @@ def run_ours(args, world, rank, local):
             "rooflines": rooflines,
             "gpu_launches": launches_per_step * K_steps,
             "e2e": {"value": round(e2e_us, 2), "unit": "us", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "copies": "inside the captured step: copy kernels over the chip-to-chip "
+                              "link in the launch chain (q before layer 0, the last two "
+                              "layers' outputs after the last) and copy-engine copies on a "
+                              "second stream (the other outputs, every 8 layers; q rows "
+                              "beyond 1 MiB beside layer 0)"},
             "clocks": clocks.summary(),
             "wall_s_pass1": round(wall_ppsa, 3),
         }

@@ -282,13 +282,21 @@ void td_plan_destroy(td_plan *plan);
  * call; it is the plumbing around the step.  Every layer's q rows and
  * outputs live in one buffer per side:
  *   q_host    HOST, page-locked (cudaHostAlloc / cudaHostRegister), bf16
- *             [num_layers][B][Hq][128]: copied to q in one copy at the start
- *             of the step.
+ *             [num_layers][B][Hq][128]: copied to q at the start of the step.
  *   q         DEVICE bf16 [num_layers][B][Hq][128]: layer l reads q + l*B*Hq*128.
  *   outs      DEVICE bf16 [num_layers][B][Hq][128]: layer l writes outs + l*B*Hq*128.
- *   out_host  HOST, page-locked, bf16 [num_layers][B][Hq][128]: receives outs;
- *             layers 0 .. L-2 in one copy on a second stream of the graph
- *             while the last layer runs, the last layer's after it.
+ *   out_host  HOST, page-locked, bf16 [num_layers][B][Hq][128]: receives outs.
+ * When both host buffers are mapped into the device's address space (as
+ * page-locked memory is under unified addressing) and every buffer is
+ * 16-byte aligned, kernels of the step copy over the chip-to-chip link in
+ * its launch chain: q before layer 0 (beyond 1 MiB only layer 0's rows, the
+ * rest by the copy engines on a second stream of the graph beside layer 0),
+ * the outputs of every 8 layers by the copy engines on the second stream as
+ * the step goes, the last two layers' by a kernel after the last layer.
+ * Otherwise (or with the tuning key "host_copy" = 0 at creation) the copy
+ * engines move them all: q in one copy before layer 0, the outputs of layers
+ * 0 .. L-2 on the second stream while the last layer runs, the last layer's
+ * after it.
  * Other arguments as in td_plan_create (outs_f32 stay on the device).
  * Pageable host memory is rejected with TD_ERR_INVALID_ARG (nothing
  * captured).  Each host range must lie in one page-locked allocation.  The
@@ -361,6 +369,10 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          register-streamed sparse kernels that fit 4 or more per SM are
  *          planned one below it, leaving room for the next layer's CTAs)
  *   "full_waves", "sparse_waves": target waves of CTAs per launch
+ *   "host_copy": 1 (default) host-buffer plans created afterwards copy with
+ *          kernels where the host buffers are mapped; 0 with the copy
+ *          engines only (see td_plan_create_host); other values restore the
+ *          default
  *   "sparse_splits": 1..256 splits per (batch, KV head) of sparse launches
  *          (then kept within "max_splits", at most one per 64 entries, and
  *          at least one per 2048 entries, the most a sparse CTA stages);

@@ -68,6 +68,8 @@ struct Tuning {
     // 3844 / 3841 / 3826 / 3813 / - / 3808 us, 10K 282.5 -> 280.4 us (4, with
     // the cp.async-staged sparse layers).
     int early_trigger = 4;
+    int host_copy = 1;           // host-buffer plans: 1 copy kernels in the launch chain (see
+                                 // StepIo), 0 copy-engine copies only
     int wait_limit_us = 0;       // staged full layers: microseconds a stage wait may take before it
                                  // gives up and the launch reports TD_FLAG_WAIT_TIMEOUT (0: 1 s)
     int wait_test = 0;           // 1: each staged full-layer CTA's first wait polls a barrier that
@@ -657,14 +659,25 @@ td_status validate_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
 }
 
 // Host input/output of a captured step (td_plan_create_host), every layer's
-// rows in one buffer per side: one q copy on the step's stream before layer
-// 0; the outputs of layers 0 .. L-2 in one copy on a side stream once layer
-// L-2 is done (it overlaps the last layer), the last layer's on the step's
-// stream.  ev: 2 events created by the caller.  Measured on GB300 against
-// copies around the plain plan: serving batch e2e 1942 -> 1918 us, 32K
-// 779 -> 776 us, 100K 1438 -> 1436 us, 10K 301 -> 304 us; one copy per
-// layer costs 20-100 us a step, and per-layer waits on the q copies break
-// the programmatic launches between layers (32K +150 us).
+// rows in one buffer per side.  With copy kernels (host_copy 1, the default,
+// when both host buffers are mapped): the q rows by a kernel ahead of layer 0
+// in the programmatic launch chain (layer 0's CTAs launch while it runs) --
+// above 1 MiB only layer 0's, the rest by the copy engines on a side stream
+// beside layer 0, which layer 1 waits for; the outputs of every 8 layers by
+// the copy engines on the side stream once their last layer is done; the
+// last two layers' by a kernel after the last layer, then the side stream is
+// joined.  Copy engines only (host_copy 0, or unmapped buffers): one q copy
+// before layer 0, the outputs of layers 0 .. L-2 once layer L-2 is done, the
+// last layer's after it.  Measured on GB300 (graph steps, e2e against the
+// same step on device buffers): copy kernels 100K 1398.9 / 1399.8 us, 32K
+// 743.3 / 738.7, serving batch k = 1024 1787.6 / 1770.3, 10K 281.0 / 279.5;
+// copy engines 1417.7, 760.2, 1850.5, 297.8 us.  Also measured: copy kernels
+// with one output copy on the side stream after layer L-2 (1400.3, 746.6,
+// 1843.1, 284.0 us: at 10K the copy is not hidden by the short last layer),
+// all outputs by the tail kernel (1399.1, 749.8, 1861.9, 279.7 us), chunked
+// outputs without the q split (1399.3, 743.6, 1816.6, 280.7 us).  One copy
+// per layer costs 20-100 us a step, and a wait on a q copy before every layer
+// breaks the programmatic launches between layers (32K +150 us).
 struct StepIo {
     const void *q_host;
     void *q;
@@ -673,7 +686,61 @@ struct StepIo {
     size_t layer_bytes;  // B * Hq * 128 * 2
     cudaStream_t stream;
     cudaEvent_t *ev;
+    // device addresses of the two host buffers (page-locked host memory is
+    // mapped into the device's address space): the copies run as kernels
+    // when both are set and every buffer is 16-byte aligned
+    const void *q_host_dev;
+    void *out_host_dev;
+    int mode;  // host_copy tuning at capture
 };
+
+constexpr size_t kSplitQBytes = size_t(1) << 20;  // q rows above this come in beside layer 0
+constexpr int kOutChunkLayers = 8;                // layers per side-stream output copy
+
+// Copies n 16-byte words between host and device memory, read or written by
+// the SMs over the chip-to-chip link.  As a kernel it takes part in the
+// step's programmatic launch chain: it waits for the kernel before it (when
+// launched as a dependent), and lets the next one launch at once, so that
+// kernel's CTAs request their first cache rows while the copy runs.
+__global__ void __launch_bounds__(256) io_copy_kernel(const uint4 *__restrict__ src,
+                                                      uint4 *__restrict__ dst, size_t n)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {  // four loads in flight per thread
+        const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride],
+                    d = src[i + 3 * stride];
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = d;
+    }
+    for (; i < n; i += stride)
+        dst[i] = src[i];
+}
+
+cudaError_t launch_io_copy(const void *src, void *dst, size_t bytes, bool pdl, cudaStream_t st)
+{
+    const size_t n = bytes / 16;
+    if (n == 0)
+        return cudaSuccess;
+    long grid = (long)ceil_div((long)n, 256);
+    const long most = 4L * device_sm_count();
+    if (grid > most)
+        grid = most;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, io_copy_kernel, (const uint4 *)src, (uint4 *)dst, n);
+}
 
 td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
                        const void *const *q, const void *const *k_caches,
@@ -697,12 +764,41 @@ td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
                                  c.shape.max_seq_len, st) != cudaSuccess)
             return TD_ERR_CUDA;
     }
-    // host inputs: every layer's q rows before layer 0
-    if (io && cudaMemcpyAsync(io->q, io->q_host, io->layer_bytes * num_layers,
-                              cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return TD_ERR_CUDA;
+    // Host rows (see StepIo): which layers' outputs the tail copy takes, how
+    // many layers each side-stream output copy takes, and whether the q rows
+    // of layers 1 .. L-1 come in on the side stream beside layer 0.
+    const bool io_kernels = io && io->mode > 0 && io->q_host_dev && io->out_host_dev;
+    const int L = num_layers;
+    const size_t lb = io ? io->layer_bytes : 0;
+    int tail_from = L - 1, chunk = L;
+    bool q_split = false;
+    if (io_kernels) {
+        tail_from = L >= 2 ? L - 2 : 0;
+        chunk = kOutChunkLayers;
+        q_split = L >= 2 && lb * L > kSplitQBytes;
+    }
+    if (io) {
+        if (q_split) {
+            if (cudaEventRecord(io->ev[0], st) != cudaSuccess ||
+                cudaStreamWaitEvent(io->stream, io->ev[0], 0) != cudaSuccess ||
+                cudaMemcpyAsync((char *)io->q + lb, (const char *)io->q_host + lb, lb * (L - 1),
+                                cudaMemcpyHostToDevice, io->stream) != cudaSuccess ||
+                cudaEventRecord(io->ev[1], io->stream) != cudaSuccess ||
+                launch_io_copy(io->q_host_dev, io->q, lb, false, st) != cudaSuccess)
+                return TD_ERR_CUDA;
+        } else if ((io_kernels ? launch_io_copy(io->q_host_dev, io->q, lb * L, false, st)
+                               : cudaMemcpyAsync(io->q, io->q_host, lb * L, cudaMemcpyHostToDevice,
+                                                 st)) != cudaSuccess) {
+            return TD_ERR_CUDA;
+        }
+    }
+    int side_from = 0, n_side = 0;
+    bool side_used = q_split;
     for (int l = 0; l < num_layers; ++l) {
-        const bool pdl = l > 0 && g_tuning.pdl;  // the first kernel waits for what precedes it
+        // the first kernel waits for what precedes it, except a copy kernel
+        const bool pdl = (l > 0 || io_kernels) && g_tuning.pdl;
+        if (q_split && l == 1 && cudaStreamWaitEvent(st, io->ev[1], 0) != cudaSuccess)
+            return TD_ERR_CUDA;
         if (layer_events && layer_events[l] &&
             cudaEventRecord((cudaEvent_t)layer_events[l], st) != cudaSuccess)
             return TD_ERR_CUDA;
@@ -724,21 +820,31 @@ td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
         }
         if (r)
             return r;
-        // host outputs of layers 0 .. l on the side stream once layer l = L-2 is done
-        if (io && l == num_layers - 2 &&
-            (cudaEventRecord(io->ev[0], st) != cudaSuccess ||
-             cudaStreamWaitEvent(io->stream, io->ev[0], 0) != cudaSuccess ||
-             cudaMemcpyAsync(io->out_host, io->outs, io->layer_bytes * (l + 1),
-                             cudaMemcpyDeviceToHost, io->stream) != cudaSuccess ||
-             cudaEventRecord(io->ev[1], io->stream) != cudaSuccess))
-            return TD_ERR_CUDA;
+        // host outputs of layers side_from .. l on the side stream once layer l is done
+        if (io && l < tail_from && (l + 1 - side_from == chunk || l == tail_from - 1)) {
+            cudaEvent_t e = io->ev[3 + n_side++];
+            if (cudaEventRecord(e, st) != cudaSuccess ||
+                cudaStreamWaitEvent(io->stream, e, 0) != cudaSuccess ||
+                cudaMemcpyAsync((char *)io->out_host + lb * side_from,
+                                (const char *)io->outs + lb * side_from, lb * (l + 1 - side_from),
+                                cudaMemcpyDeviceToHost, io->stream) != cudaSuccess)
+                return TD_ERR_CUDA;
+            side_from = l + 1;
+            side_used = true;
+        }
     }
-    // the last layer's output, then join the side stream
+    // the remaining layers' outputs, then join the side stream
     if (io) {
-        const size_t last = io->layer_bytes * (num_layers - 1);
-        if (cudaMemcpyAsync((char *)io->out_host + last, (const char *)io->outs + last,
-                            io->layer_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-            (num_layers >= 2 && cudaStreamWaitEvent(st, io->ev[1], 0) != cudaSuccess))
+        const size_t first = lb * tail_from, bytes = lb * (L - tail_from);
+        const cudaError_t e =
+            io_kernels ? launch_io_copy((const char *)io->outs + first,
+                                        (char *)io->out_host_dev + first, bytes, g_tuning.pdl, st)
+                       : cudaMemcpyAsync((char *)io->out_host + first,
+                                         (const char *)io->outs + first, bytes,
+                                         cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess ||
+            (side_used && (cudaEventRecord(io->ev[2], io->stream) != cudaSuccess ||
+                           cudaStreamWaitEvent(st, io->ev[2], 0) != cudaSuccess)))
             return TD_ERR_CUDA;
     }
     if (layer_events && layer_events[num_layers] &&
@@ -793,7 +899,7 @@ td_status create_plan(td_plan **plan, const td_shape *shape, int32_t num_layers,
     if (!p)
         return TD_ERR_INVALID_ARG;
     const bool host_io = host != nullptr;
-    std::vector<cudaEvent_t> ev(host_io ? 2 : 0, nullptr);
+    std::vector<cudaEvent_t> ev(host_io ? 3 + num_layers : 0, nullptr);
     cudaStream_t cap = nullptr, side = nullptr;
     bool ok = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) == cudaSuccess;
     if (ok && host_io) {
@@ -1119,6 +1225,17 @@ td_status td_plan_create_host(td_plan **plan, const td_shape *shape, int32_t num
     io.outs = outs;
     io.out_host = out_host;
     io.layer_bytes = (size_t)shape->batch * shape->num_q_heads * kHeadDim * sizeof(uint16_t);
+    io.mode = g_tuning.host_copy;
+    void *dq = nullptr, *dout = nullptr;
+    if (io.mode > 0 && aligned(q_host, 16) && aligned(out_host, 16) && aligned(q, 16) &&
+        aligned(outs, 16) &&
+        cudaHostGetDevicePointer(&dq, const_cast<void *>(q_host), 0) == cudaSuccess &&
+        cudaHostGetDevicePointer(&dout, out_host, 0) == cudaSuccess) {
+        io.q_host_dev = dq;
+        io.out_host_dev = dout;
+    } else {
+        cudaGetLastError();  // not mapped: the copy engines move the rows
+    }
     std::vector<const void *> qs(num_layers);
     std::vector<void *> os(num_layers);
     for (int l = 0; l < num_layers; ++l) {
@@ -1195,6 +1312,8 @@ td_status td_set_tuning(const char *key, int32_t value)
         g_tuning.full_interleave = value > 0 ? 1 : (value == 0 ? 0 : kDefaultTuning.full_interleave);
     else if (!strcmp(key, "early_trigger"))
         g_tuning.early_trigger = (value >= 0 && value <= 64) ? value : kDefaultTuning.early_trigger;
+    else if (!strcmp(key, "host_copy"))
+        g_tuning.host_copy = (value == 0 || value == 1) ? value : kDefaultTuning.host_copy;
     else if (!strcmp(key, "wait_limit_us"))
         g_tuning.wait_limit_us = value > 0 ? value : kDefaultTuning.wait_limit_us;
     else if (!strcmp(key, "wait_test"))

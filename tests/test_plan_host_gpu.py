@@ -2,8 +2,10 @@
 rows in from page-locked host memory and the outputs back (one buffer per
 side).  The device results must equal those of the plain plan bitwise,
 launch after launch, and the host buffer must hold exactly the device
-outputs once the stream is done.  Pageable host memory is rejected by the C
-call itself."""
+outputs once the stream is done -- with the copy kernels (the default) and
+with the copy engines, on steps whose q rows exceed 1 MiB (the rows of
+layers 1 .. L-1 come in beside layer 0) and whose outputs take several
+side-stream copies.  Pageable host memory is rejected by the C call itself."""
 import ctypes
 
 import numpy as np
@@ -23,11 +25,15 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def _workload(name):
+def _workload(name, n_layers=4):
     wl = W.WORKLOADS[name]
     if name != "tiny":   # a grouped-query workload, cut to a few layers of short rows
-        wl = wl.with_(layers=4, modes=(W.FULL, W.FULL, W.FULL_SELECT, W.SPARSE),
-                      max_seq_len=4096, top_k=512)
+        modes = (W.FULL, W.FULL, W.FULL_SELECT) + (W.SPARSE,) * (n_layers - 3)
+        if name == "serving-b32":
+            wl = wl.with_(layers=n_layers, modes=modes, max_seq_len=1024, top_k=256,
+                          ragged=(600, 1024))
+        else:
+            wl = wl.with_(layers=n_layers, modes=modes, max_seq_len=4096, top_k=512)
     heavy = W.heavy_positions(wl)
     layers = [W.generate_layer(wl, layer, "cpu", heavy[layer]) for layer in range(wl.layers)]
     return wl, layers
@@ -45,9 +51,16 @@ def _device_plan_run(wl, shape, q_rows, K, V, seq):
     return [o.cpu() for o in outs], idx.cpu()
 
 
-@pytest.mark.parametrize("name", ["tiny", "llama3-8b-32k"])
-def test_host_plan_equals_the_device_plan_on_every_launch(name):
-    wl, layers = _workload(name)
+# (workload, layers): 12 layers of the 32K shape take output copies of
+# layers 0-7 and 8-9 on the side stream; 6 layers of the serving batch hold
+# 1.5 MiB of q rows
+CASES = [("tiny", 4), ("llama3-8b-32k", 12), ("serving-b32", 6)]
+
+
+@pytest.mark.parametrize("host_copy", [1, 0], ids=["kernels", "engines"])
+@pytest.mark.parametrize("name,n_layers", CASES, ids=[c[0] for c in CASES])
+def test_host_plan_equals_the_device_plan_on_every_launch(name, n_layers, host_copy):
+    wl, layers = _workload(name, n_layers)
     shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len)
     K = [x[1].cuda() for x in layers]
     V = [x[2].cuda() for x in layers]
@@ -59,8 +72,12 @@ def test_host_plan_equals_the_device_plan_on_every_launch(name):
     out_host = torch.full(rows_shape, float("nan"), dtype=torch.bfloat16).pin_memory()
     idx = torch.full((wl.batch, wl.kv_heads, wl.top_k), -1, dtype=torch.int32, device="cuda")
     ws = td.Workspace(shape, wl.top_k)
-    plan = td.Plan(shape, wl.modes, list(q_all.unbind(0)), K, V, seq, wl.top_k, idx,
-                   list(outs_all.unbind(0)), None, ws, q_host=q_host, out_host=out_host)
+    td.td_set_tuning("host_copy", host_copy)
+    try:
+        plan = td.Plan(shape, wl.modes, list(q_all.unbind(0)), K, V, seq, wl.top_k, idx,
+                       list(outs_all.unbind(0)), None, ws, q_host=q_host, out_host=out_host)
+    finally:
+        td.td_set_tuning("host_copy", -1)
     rs = np.random.RandomState(5)
     for launch in range(3):
         if launch > 0:   # new host q rows for this launch
