@@ -33,7 +33,7 @@ struct Tuning {
                                  // CTAs per SM and waves above)
     int max_splits = td::kMaxSplits;
     int cluster = 0;             // 1: merge up to kPortableClusterSplits splits through a cluster
-    int topk_threads = 0;        // 0 = 1024 threads per row, or 512
+    int topk_threads = 0;        // 1024 or 512 threads per row; 0: automatic (topk_threads_for)
     int full_staged = -1;        // 1: full / full+select kernels stage K/V through shared memory
                                  // (bulk copies); 0: register-streamed; -1: staged when G >= 4
     int sparse_staged = -1;      // CUDA-core sparse kernels: 1 stage the gathered rows through
@@ -403,6 +403,35 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
     chunk = (int)ch;
 }
 
+// Threads per top-k CTA of a selection over this shape (one CTA per row);
+// next_mode: the mode of the layer launched right after it in the same call
+// (-1: none).  Measured on GB300 (serving batch, 256 rows of 8K-16K scores,
+// graph steps): 512-thread CTAs, two per SM, take the rows in one wave
+// instead of 1.7, k = 1024 1769.8 -> 1754.1 us, k = 4096 3789.0 -> 3774.5
+// us.  But two 512-thread CTAs leave no registers for the next kernel's
+// early-launched CTAs: before the 8-token sparse kernel (k = 256) the step
+// goes 1281.5 -> 1340.6 us, and before full layers (selection at every
+// layer) 8681 -> 10648 us.  Rows that fit one wave of 1024-thread CTAs keep
+// them.
+int topk_threads_for(const td_shape &s, int top_k, int next_mode)
+{
+    if (g_tuning.topk_threads > 0)
+        return g_tuning.topk_threads;
+    const long rows = (long)s.batch * s.num_kv_heads;
+    if (rows <= device_sm_count())
+        return 1024;
+    if (next_mode < 0)
+        return 512;
+    if (next_mode != TD_MODE_SPARSE)
+        return 1024;
+    int nsplit = 0, chunk = 0;
+    plan_splits(s, top_k, true, false, nsplit, chunk);
+    const int G = s.num_q_heads / s.num_kv_heads;
+    return (mma_for(G) && g_tuning.sparse_stream_k <= 0 && mma_tokens_for(true, chunk, nsplit) == 64)
+               ? 512
+               : 1024;
+}
+
 struct Ctx {
     td_shape shape;
     int G;
@@ -482,7 +511,7 @@ struct Coverage {
 td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
                    const int32_t *seq_lens, int top_k, int32_t *idx_out, void *out,
                    float *out_f32, float *scores_out, cudaStream_t st, bool pdl,
-                   Coverage cov = Coverage{})
+                   Coverage cov = Coverage{}, int next_mode = -1)
 {
     const bool select = top_k > 0;
     td::AttnArgs a = base_args(c, q, k, v, seq_lens, out, out_f32);
@@ -533,8 +562,9 @@ td_status run_full(const Ctx &c, const void *q, const void *k, const void *v,
             t.row_k = ca.row_k;
             t.counts = cov.counts;
         }
-        if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, topk_cluster_for(c.shape),
-                            g_tuning.pdl != 0 && g_tuning.topk_pdl != 0, st) != cudaSuccess)
+        if (td::launch_topk(t, c.shape.batch, topk_threads_for(c.shape, top_k, next_mode),
+                            topk_cluster_for(c.shape), g_tuning.pdl != 0 && g_tuning.topk_pdl != 0,
+                            st) != cudaSuccess)
             return TD_ERR_CUDA;
     }
     return TD_OK;
@@ -811,7 +841,8 @@ td_status enqueue_step(const Ctx &c, int32_t num_layers, const int32_t *modes,
             break;
         case TD_MODE_FULL_SELECT:
             r = run_full(c, q[l], k_caches[l], v_caches[l], seq_lens, top_k, idx_buf,
-                         outs[l], of, nullptr, st, pdl);
+                         outs[l], of, nullptr, st, pdl, Coverage{},
+                         l + 1 < num_layers ? modes[l + 1] : -1);
             break;
         default:
             r = run_sparse(c, q[l], k_caches[l], v_caches[l], seq_lens, idx_buf, top_k,
@@ -1060,8 +1091,8 @@ td_status td_topk_select(const td_shape *shape, const float *scores, const int32
     t.Nmax = c.shape.max_seq_len;
     t.top_k = top_k;
     t.warp_select_max = g_tuning.topk_warp_max;
-    if (td::launch_topk(t, c.shape.batch, g_tuning.topk_threads, topk_cluster_for(c.shape), false,
-                        (cudaStream_t)stream) != cudaSuccess)
+    if (td::launch_topk(t, c.shape.batch, topk_threads_for(c.shape, top_k, -1),
+                        topk_cluster_for(c.shape), false, (cudaStream_t)stream) != cudaSuccess)
         return TD_ERR_CUDA;
     return TD_OK;
 }
