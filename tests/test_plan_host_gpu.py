@@ -27,7 +27,9 @@ def _built():
 
 def _workload(name, n_layers=4):
     wl = W.WORKLOADS[name]
-    if name != "tiny":   # a grouped-query workload, cut to a few layers of short rows
+    if name == "tiny" and n_layers < 4:   # one full+select layer, then at most one sparse layer
+        wl = wl.with_(layers=n_layers, modes=(W.FULL_SELECT, W.SPARSE)[:n_layers])
+    elif name != "tiny":   # a grouped-query workload, cut to a few layers of short rows
         modes = (W.FULL, W.FULL, W.FULL_SELECT) + (W.SPARSE,) * (n_layers - 3)
         if name == "serving-b32":
             wl = wl.with_(layers=n_layers, modes=modes, max_seq_len=1024, top_k=256,
@@ -53,12 +55,12 @@ def _device_plan_run(wl, shape, q_rows, K, V, seq):
 
 # (workload, layers): 12 layers of the 32K shape take output copies of
 # layers 0-7 and 8-9 on the side stream; 6 layers of the serving batch hold
-# 1.5 MiB of q rows
-CASES = [("tiny", 4), ("llama3-8b-32k", 12), ("serving-b32", 6)]
+# 1.5 MiB of q rows; one and two layers leave the side stream unused
+CASES = [("tiny", 4), ("tiny", 1), ("tiny", 2), ("llama3-8b-32k", 12), ("serving-b32", 6)]
 
 
 @pytest.mark.parametrize("host_copy", [1, 0], ids=["kernels", "engines"])
-@pytest.mark.parametrize("name,n_layers", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("name,n_layers", CASES, ids=[f"{c[0]}-L{c[1]}" for c in CASES])
 def test_host_plan_equals_the_device_plan_on_every_launch(name, n_layers, host_copy):
     wl, layers = _workload(name, n_layers)
     shape = td.make_shape(wl.batch, wl.q_heads, wl.kv_heads, wl.max_seq_len)
