@@ -419,7 +419,7 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          of "topk_threads"), or 2, 4, 8 (a thread-block cluster of
  *          1024-thread CTAs, each scanning a slice of the row, merged through
  *          distributed shared memory); other values restore the default
- *          (for rows of at least 65536 positions, the largest cluster for
+ *          (for rows of at least 32768 positions, the largest cluster for
  *          which rows x cluster fits one wave of SMs with at least 16384
  *          positions per CTA; else 1)
  *   "pdl", "topk_pdl": 0 turns off programmatic dependent launch between a
