@@ -300,12 +300,12 @@ int device_sm_count();
 // are long (at least kMinClusterRow positions), few enough for rows x CS CTAs
 // to fit one wave, and each CTA still scans at least kMinClusterSlice
 // positions; else one CTA per row.  Measured on GB300 (graph step): clusters
-// of 4 take 10 us off each 100K selection layer (2: 1401.8 -> 1423.1 us a
-// step); at 10K they cost 4.6 us a step, since the cluster's CTAs fill their
-// SMs and the next layer's CTAs cannot start early beside them.  At 32K they
-// cost 5-19 us while the sparse layers after them were planned with a CTA
-// for every slot; with the whole-round sparse plan, which leaves slots free,
-// clusters of 2 take 739.3 -> 730.9 us (4: 731.9 us).
+// of 4 take 10 us off each 100K selection layer (clusters of 2 instead: step
+// 1401.8 -> 1423.1 us); at 10K they cost 4.6 us a step, since the cluster's
+// CTAs fill their SMs and the next layer's CTAs cannot start early beside
+// them.  At 32K they cost 5-19 us while the sparse layers after them were
+// planned with a CTA for every slot; with the whole-round sparse plan, which
+// leaves slots free, clusters of 2 take 739.3 -> 730.9 us (4: 731.9 us).
 constexpr int kMinClusterRow = 32768;
 constexpr int kMinClusterSlice = 16384;
 int topk_cluster_for(const td_shape &s)
