@@ -136,7 +136,7 @@ def test_tuning_keys(L):
     td.td_set_tuning("topk_warp_max", 0)
     for key, value in (("mma_full_tokens", 8), ("mma_sparse_tokens", 32), ("mma_sparse_tokens", 64),
                        ("topk_cluster", 4), ("sparse_staged", 2), ("full_interleave", 0),
-                       ("early_trigger", 0), ("sparse_splits", 5),
+                       ("early_trigger", 0), ("sparse_splits", 5), ("host_copy", 0),
                        ("wait_limit_us", 50), ("wait_test", 1)):
         td.td_set_tuning(key, value)
         td.td_set_tuning(key, -1 if key not in ("wait_limit_us", "wait_test") else 0)
