@@ -271,13 +271,23 @@ def load_measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def attn_source_hash() -> str:
-    """Hash of the attention kernels' code (comments and whitespace removed,
-    so that an edit to a comment does not retire the DRAM traffic ncu
-    measured on the same code)."""
+# The sources each attention kernel family is built from: the CUDA-core
+# kernels (attention_kernel) and the tensor-core ones (attention_mma*).
+ATTN_SOURCES = {"cuda": ("td_attn.cu", "td_attn_common.cuh", "td_internal.h"),
+                "mma": ("td_attn_mma.cu", "td_attn_common.cuh", "td_internal.h")}
+
+
+def kernel_family(kernel: str) -> str:
+    return "mma" if kernel.startswith("attention_mma") else "cuda"
+
+
+def attn_source_hash(family: str) -> str:
+    """Hash of one attention kernel family's code (comments and whitespace
+    removed, so that an edit to a comment does not retire the DRAM traffic
+    ncu measured on the same code)."""
     import re
     h = hashlib.sha256()
-    for name in ("td_attn.cu", "td_attn_mma.cu", "td_attn_common.cuh", "td_internal.h"):
+    for name in ATTN_SOURCES[family]:
         with open(os.path.join(ROOT, "sparse_attention_td_gb300", "csrc", name)) as f:
             src = f.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
@@ -297,7 +307,8 @@ def measured_traffic(workload: str, kernel: str):
     except (OSError, ValueError):
         return None
     entry = rec.get(f"{workload}:{kernel}")
-    if not entry or entry.get("source_hash") != attn_source_hash():
+    if not entry or entry.get("source_hash") != attn_source_hash(
+            kernel_family(entry.get("kernel", ""))):
         return None
     return entry.get("dram_bytes_per_launch")
 

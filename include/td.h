@@ -429,11 +429,10 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *          8 (CTAs of 8 warps) or 16 (CTAs of 4 warps, both row groups of the
  *          MMA); 32 takes 16 per round with two rounds in flight per warp
  *          (the next round requested before this one's arithmetic); 64
- *          (sparse only) stages a CTA's rounds in a ring of shared-memory
- *          buffers, two rounds in flight ahead of the one computed; defaults
- *          16 for full layers; for sparse layers 64 when a CTA gathers at
- *          least 1024 rows or a (batch row, KV head) is split over several
- *          CTAs, else 8; other values restore the default
+ *          (sparse only) stages a CTA's rounds in a ring of two
+ *          shared-memory buffers, one round in flight ahead of the one
+ *          computed; defaults 16 for full layers and 64 for sparse layers;
+ *          other values restore the default
  *   "early_trigger": rounds before the end of its last round at which a
  *          CTA (ring, register-streamed, cp.async-staged sparse and 16-token
  *          full kernels) lets the

@@ -52,8 +52,7 @@ struct Tuning {
     int mma_full_tokens = 16;    // tensor-core full / full+select kernels: tokens per warp per round
     int mma_sparse_tokens = 0;   // tensor-core sparse kernels: tokens per warp per round (8, 16, or
                                  // 32 = 16 with two rounds in flight, 64 = rounds staged in shared
-                                 // memory); 0: 64 when a CTA's chunk holds >= kLongSparseChunk
-                                 // entries or a pair has several splits, else 8
+                                 // memory); 0: 64
     int full_interleave = 1;     // full layers (tensor cores with 16 tokens per warp, or CUDA cores
                                  // register-streamed): 1 the splits of a (batch row, KV head)
                                  // take its 64-token rounds in turn, 0 one contiguous chunk each
@@ -96,25 +95,26 @@ int prefetch_for(int G)
 }
 
 // Measured on GB300 (graph steps): sparse layers staged through the
-// shared-memory ring (its first two rounds requested before the wait for the
-// previous kernel) beat the 8-token register kernel where a pair's rows are
-// split over several CTAs (32K: 765 -> 756 us, the prefetch overlaps the
-// split merge of the layer before) and where CTAs gather >= 1024 rows
-// (serving batch k = 1024: 1861 -> 1830 us; k = 4096: 4094 -> 3954 us, also
-// ahead of the 16-token kernel with two rounds in flight); on one-split
-// layers of 256-row CTAs (serving batch k = 256) they lose 0.4-3 us a layer.
-constexpr int kLongSparseChunk = 1024;
+// shared-memory ring (its first round requested before the wait for the
+// previous kernel) beat the 8-token register kernel on every grouped-query
+// workload once the ring has two stages: serving batch k = 256 (one 256-row
+// CTA per pair) 1279.8 -> 1237.5 us.  With three stages the ring won only
+// where a pair's rows are split over several CTAs (32K: 765 -> 756 us) or
+// CTAs gather >= 1024 rows (serving k = 1024: 1861 -> 1830 us; k = 4096:
+// 4094 -> 3954 us) and lost 0.4-3 us a layer at k = 256.
 
 // Tokens per warp per round of a tensor-core launch (64: the sparse ring
 // kernel); chunk and nsplit: index entries per CTA and splits per (batch
 // row, KV head) of a sparse launch (the split plan is the same for 8 and 64).
 int mma_tokens_for(bool sparse, int chunk = 0, int nsplit = 1)
 {
+    (void)chunk;
+    (void)nsplit;
     if (!sparse)
         return g_tuning.mma_full_tokens;
     if (g_tuning.mma_sparse_tokens > 0)
         return g_tuning.mma_sparse_tokens;
-    return (chunk >= kLongSparseChunk || nsplit > 1) ? 64 : 8;
+    return 64;
 }
 
 int device_sm_count();
@@ -408,14 +408,15 @@ void plan_splits(const td_shape &s, long n_total, bool sparse, bool select, int 
 
 // Threads per top-k CTA of a selection over this shape (one CTA per row);
 // next_mode: the mode of the layer launched right after it in the same call
-// (-1: none).  Measured on GB300 (serving batch, 256 rows of 8K-16K scores,
-// graph steps): 512-thread CTAs, two per SM, take the rows in one wave
-// instead of 1.7, k = 1024 1769.8 -> 1754.1 us, k = 4096 3789.0 -> 3774.5
-// us.  But two 512-thread CTAs leave no registers for the next kernel's
-// early-launched CTAs: before the 8-token sparse kernel (k = 256) the step
-// goes 1281.5 -> 1340.6 us, and before full layers (selection at every
-// layer) 8681 -> 10648 us.  Rows that fit one wave of 1024-thread CTAs keep
-// them.
+// (-1: none).  512-thread CTAs, two per SM, take more rows than SMs in one
+// wave (a lone launch: 68.2 -> 65.0 us on the serving batch), but they leave
+// no registers for the next kernel's CTAs to start early beside them, which
+// matters unless that kernel needs more than one wave of CTAs anyway.
+// Measured on GB300 (serving batch, two-stage sparse ring, graph steps): 1024
+// threads against 512 at k = 256 1237.3 / 1301.6 us and k = 1024 1695.2 /
+// 1750.7 us (one wave of sparse CTAs after them); at k = 4096 (two splits a
+// pair, 1.7 waves) 3776.8 / 3757.7 us; before full layers (selection at
+// every layer) 8681 / 10648 us.
 int topk_threads_for(const td_shape &s, int top_k, int next_mode)
 {
     if (g_tuning.topk_threads > 0)
@@ -430,9 +431,11 @@ int topk_threads_for(const td_shape &s, int top_k, int next_mode)
     int nsplit = 0, chunk = 0;
     plan_splits(s, top_k, true, false, nsplit, chunk);
     const int G = s.num_q_heads / s.num_kv_heads;
-    return (mma_for(G) && g_tuning.sparse_stream_k <= 0 && mma_tokens_for(true, chunk, nsplit) == 64)
-               ? 512
-               : 1024;
+    int per_sm = g_tuning.sparse_ctas_per_sm;
+    if (per_sm <= 0)
+        per_sm = mma_for(G) ? td::attention_mma_ctas_per_sm(G, true, false, mma_tokens_for(true))
+                            : td::attention_ctas_per_sm(G, true, false, staged_for(s, true, top_k));
+    return rows * nsplit > (long)device_sm_count() * per_sm ? 512 : 1024;
 }
 
 struct Ctx {

@@ -9,12 +9,11 @@
 // Three kernels, the same arithmetic, different tiling:
 //   * attention_mma_kernel: a warp takes 8 tokens per round (MMA rows 8..15
 //     of S and tokens 8..15 of the P V k-step stay zero), a CTA of 8 warps
-//     64 tokens; 2 CTAs per SM.  Default for sparse layers of one short CTA
-//     per (batch row, KV head).
+//     64 tokens; 2 CTAs per SM.
 //   * attention_mma_ring_kernel: the same 8-token rounds for sparse layers,
-//     gathered into a ring of shared-memory stages by cp.async and read back
-//     by ldmatrix, two rounds in flight ahead of the one computed.  Default
-//     for the other sparse layers.
+//     gathered into a ring of two shared-memory stages by cp.async and read
+//     back by ldmatrix, one round in flight ahead of the one computed.
+//     Default for sparse layers.
 //   * attention_mma16_kernel: a warp takes 16 tokens per round (rows r and
 //     r + 8 of S are two tokens, the P V k-step takes all 16), a CTA of 4
 //     warps 64 tokens; half the MMAs and shuffles per token, 3 CTAs per SM.
@@ -362,10 +361,14 @@ attention_mma_kernel(const AttnArgs a)
 //     dims 16t + r / 16t + 8 + r, k = the warp's 8 tokens (8..15 zero);
 //     B = P^T as in attention_mma_kernel.
 // The warps' partial outputs reuse the ring once the last round is done.
-constexpr int kRingStages = 3;
+// Measured on GB300 (graph steps, outputs bitwise equal): two stages against
+// three take 32K 730.8 -> 688.2 us, serving batch k = 1024 1751.7 -> 1697.1
+// us, and at k = 256 the ring beats the 8-token kernel, 1279.8 -> 1237.5 us
+// (three stages: 1314.5 us).
+constexpr int kRingStages = 2;
 constexpr int kRingRowBytes = kHeadDim * 2;                          // 256
 constexpr int kRingStageBytes = 2 * kTokPerRound * kRingRowBytes;    // K block + V block
-constexpr int kRingSmemBytes = kRingStages * kRingStageBytes;        // 96 KB
+constexpr int kRingSmemBytes = kRingStages * kRingStageBytes;        // 64 KB
 
 __device__ __forceinline__ uint32_t shared_addr(const void *p)
 {

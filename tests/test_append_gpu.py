@@ -34,7 +34,7 @@ PATHS = {
     "staged": {"full_staged": 1, "sparse_staged": 1, "mma": 0},
     "tma": {"full_staged": 1, "sparse_staged": 2, "mma": 0},
     "mma": {"mma": 1},
-    "mma8": {"mma": 1, "mma_full_tokens": 8, "full_prefetch": 2},
+    "mma8": {"mma": 1, "mma_full_tokens": 8, "mma_sparse_tokens": 8, "full_prefetch": 2},
     "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},
     "mma32": {"mma": 1, "mma_full_tokens": 32, "mma_sparse_tokens": 32},
     "ring": {"mma": 1, "mma_sparse_tokens": 64},

@@ -1,10 +1,8 @@
 """The kernel variant each layer kind takes by default, as td_kernel_name
 reports it on the device: the automatic choices follow the measured rules
-(tensor cores for G = 4, 8 with 16 tokens per warp on full layers; on sparse
-layers the shared-memory ring when a (batch row, KV head) is split over
-several CTAs or a CTA gathers 1024+ rows, else 8 tokens per warp; CUDA cores
-for G = 1, 2 with rows staged through cp.async when every CTA gathers one
-round or less)."""
+(tensor cores for G = 4, 8 with 16 tokens per warp on full layers and the
+shared-memory ring on sparse layers; CUDA cores for G = 1, 2 with rows staged
+through cp.async when every CTA gathers one round or less)."""
 import pytest
 import torch
 
@@ -23,11 +21,11 @@ def _built():
 def test_default_kernel_choices():
     gqa = td.make_shape(4, 32, 8, 32768)
     assert td.td_kernel_name(gqa, 0, False).startswith("attention_mma16_kernel (tensor cores, 16 tokens per warp)")
-    assert td.td_kernel_name(gqa, 2048, True).startswith("attention_mma_ring_kernel")  # 9 splits
+    assert td.td_kernel_name(gqa, 2048, True).startswith("attention_mma_ring_kernel")  # 8 splits
     serving = td.make_shape(32, 32, 8, 16384)
     assert td.td_kernel_name(serving, 4096, True).startswith("attention_mma_ring_kernel")
     assert td.td_kernel_name(serving, 1024, True).startswith("attention_mma_ring_kernel")
-    assert td.td_kernel_name(serving, 256, True).startswith("attention_mma_kernel (tensor cores, 8 tokens")
+    assert td.td_kernel_name(serving, 256, True).startswith("attention_mma_ring_kernel")
     mha = td.make_shape(1, 32, 32, 10240)
     assert "cp.async" in td.td_kernel_name(mha, 512, True)          # 32 x 512 rows: one round a CTA
     assert "register-streamed" in td.td_kernel_name(mha, 0, False)

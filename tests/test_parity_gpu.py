@@ -31,7 +31,7 @@ PATHS = {
     "staged": {"full_staged": 1, "sparse_staged": 1, "mma": 0},
     "tma": {"full_staged": 1, "sparse_staged": 2, "mma": 0},
     "mma": {"mma": 1},
-    "mma8": {"mma": 1, "mma_full_tokens": 8, "full_prefetch": 2},
+    "mma8": {"mma": 1, "mma_full_tokens": 8, "mma_sparse_tokens": 8, "full_prefetch": 2},
     "mma16": {"mma": 1, "mma_sparse_tokens": 16, "full_prefetch": 2},
     "mma32": {"mma": 1, "mma_full_tokens": 32, "mma_sparse_tokens": 32},
     "ring": {"mma": 1, "mma_sparse_tokens": 64},
@@ -49,8 +49,9 @@ def staged(request):
     (bulk copies for full layers; per-thread cp.async, or TMA row gathers, for
     sparse layers), and the tensor-core kernels (grouped-query layers with G = 4, 8; other
     groups keep the CUDA-core kernels) in three tilings: the default (16
-    tokens per warp per round for full and full+select layers, 8 for sparse
-    layers), 8 tokens per warp for every layer kind, and 16 for every layer
+    tokens per warp per round for full and full+select layers, the
+    shared-memory ring for sparse layers), 8 tokens per warp for every layer
+    kind, and 16 for every layer
     kind, these two also prefetching two rounds ahead into L2 on full layers
     (the default is one round); 16 tokens per warp with two rounds in
     flight per warp for every layer kind; sparse layers staged through a
