@@ -69,3 +69,30 @@ def test_dist_max_over_two_gloo_ranks():
 
 def test_single_rank_is_identity():
     assert bench.dist_max(3.25, 1) == 3.25
+
+
+def test_traffic_records_follow_their_kernel_family(tmp_path, monkeypatch):
+    """A committed DRAM-traffic record counts only while the sources of its
+    own kernel family are unchanged: CUDA-core records are keyed to the
+    CUDA-core sources, tensor-core records to the tensor-core ones."""
+    assert bench.kernel_family("attention_kernel<1, 1, 0, 0, 0>") == "cuda"
+    assert bench.kernel_family("attention_mma_ring_kernel<4>") == "mma"
+    assert bench.kernel_family("attention_mma16_kernel<4, 0, 0, 0, 0>") == "mma"
+    h_cuda, h_mma = bench.attn_source_hash("cuda"), bench.attn_source_hash("mma")
+    assert h_cuda != h_mma and len(h_cuda) == len(h_mma) == 16
+    rec = {
+        "w:full": {"kernel": "attention_kernel<1, 0, 0, 0, 0>", "source_hash": h_cuda,
+                   "dram_bytes_per_launch": 123},
+        "w:sparse": {"kernel": "attention_mma_ring_kernel<4>", "source_hash": h_cuda,
+                     "dram_bytes_per_launch": 456},  # keyed to the wrong family
+        "v:sparse": {"kernel": "attention_mma_ring_kernel<4>", "source_hash": h_mma,
+                     "dram_bytes_per_launch": 789},
+    }
+    f = tmp_path / "traffic.json"
+    f.write_text(__import__("json").dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.measured_traffic("w", "full") == 123
+    assert bench.measured_traffic("w", "sparse") is None
+    assert bench.measured_traffic("v", "sparse") == 789
+    assert bench.measured_traffic("v", "full") is None
+
