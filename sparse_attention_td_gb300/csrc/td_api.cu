@@ -104,12 +104,9 @@ int prefetch_for(int G)
 // 4094 -> 3954 us) and lost 0.4-3 us a layer at k = 256.
 
 // Tokens per warp per round of a tensor-core launch (64: the sparse ring
-// kernel); chunk and nsplit: index entries per CTA and splits per (batch
-// row, KV head) of a sparse launch (the split plan is the same for 8 and 64).
-int mma_tokens_for(bool sparse, int chunk = 0, int nsplit = 1)
+// kernel; the split plan is the same for every sparse tiling).
+int mma_tokens_for(bool sparse)
 {
-    (void)chunk;
-    (void)nsplit;
     if (!sparse)
         return g_tuning.mma_full_tokens;
     if (g_tuning.mma_sparse_tokens > 0)
@@ -641,7 +638,7 @@ td_status run_sparse(const Ctx &c, const void *q, const void *k, const void *v,
     }
     const cudaError_t le =
         mma_for(c.G) ? td::launch_attention_mma(c.G, true, false,
-                                                mma_tokens_for(true, a.chunk, a.nsplit), a,
+                                                mma_tokens_for(true), a,
                                                 c.shape.batch, pdl, st)
                      : td::launch_attention(c.G, true, false, cluster, staged, a,
                                             c.shape.batch, pdl, st);
@@ -1382,7 +1379,7 @@ const char *td_kernel_name(const td_shape *shape, int32_t top_k, int32_t sparse)
     if (mma_for(G)) {
         if (sp && g_tuning.sparse_stream_k > 0)
             return "attention_mma16_kernel (tensor cores, 16 tokens per warp, stream-K partition)";
-        const int t = mma_tokens_for(sp, chunk, nsplit);
+        const int t = mma_tokens_for(sp);
         return t == 64   ? "attention_mma_ring_kernel (tensor cores, rounds staged in shared memory)"
                : t == 32 ? "attention_mma16_kernel (tensor cores, 16 tokens per warp, two rounds in flight)"
                : t == 16 ? "attention_mma16_kernel (tensor cores, 16 tokens per warp)"
