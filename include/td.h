@@ -412,9 +412,9 @@ td_status td_probe_layer_reads(const td_shape *shape, const void *k_cache, const
  *   "topk_threads": 1024 or 512 threads per top-k row (512: two CTAs per
  *                   SM); other values restore the default: 512 when the
  *                   rows exceed one wave of 1024-thread CTAs (one per SM)
- *                   and nothing of the call follows the selection, or a
- *                   sparse layer on the tensor cores' shared-memory ring
- *                   does; else 1024
+ *                   and nothing of the call follows the selection, or the
+ *                   sparse layer that follows needs more than one wave of
+ *                   CTAs; else 1024
  *   "topk_cluster": CTAs per row of a top-k selection: 1 (one CTA
  *          of "topk_threads"), or 2, 4, 8 (a thread-block cluster of
  *          1024-thread CTAs, each scanning a slice of the row, merged through
